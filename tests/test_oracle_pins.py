@@ -1,0 +1,330 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself:
+closed forms, invariants of the method, special cases that reduce to a
+library routine (torch scaled_dot_product_attention, numpy matmul / sort,
+torch's float8 / bfloat16 casts) and brute force on tiny inputs.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term,
+a wrong sign or axis, an off-by-one in visibility or the window, a transposed
+operand) makes it fail."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+rng = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------- formats
+def test_bf16_decode_all_codes_match_torch():
+    u = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(u.view(np.int16)).view(torch.bfloat16).double().numpy()
+    got = O.decode_bf16(u)
+    assert np.all((np.isnan(ref) & np.isnan(got)) | (ref == got))
+
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-40, 40, 200000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.encode_bf16(x.astype(np.float64)), ref)
+
+
+def test_bf16_round_is_nearest_even_on_fp64_midpoints():
+    # values just around bf16 midpoints, below fp32 resolution: the rounding
+    # must be decided from the float64 value (no double rounding)
+    base = O.decode_bf16(rng.integers(0x3000, 0x4f00, 5000).astype(np.uint16))
+    ulp = np.ldexp(1.0, (np.floor(np.log2(base)) - 7).astype(int))
+    for off, expect_up in ((0.5 + 2.0 ** -30, True), (0.5 - 2.0 ** -30, False)):
+        r = O.round_to_bf16(base + off * ulp)
+        assert np.array_equal(r, base + ulp if expect_up else base)
+    # exact midpoints go to the even neighbour
+    r = O.round_to_bf16(base + 0.5 * ulp)
+    even = (O.encode_bf16(r) & 1) == 0
+    assert even.all()
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    u = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(u).view(torch.float8_e4m3fn).double().numpy()
+    got = O.decode_e4m3(u)
+    assert np.all((np.isnan(ref) & np.isnan(got)) | (ref == got))
+
+
+def test_e4m3_encode_matches_torch_in_range_and_saturates():
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-14, 6, 200000))).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.encode_e4m3(x.astype(np.float64)), ref)
+    big = np.array([449.0, 463.9, 464.0, 1e6, -500.0])
+    assert np.array_equal(O.decode_e4m3(O.encode_e4m3(big)), [448, 448, 448, 448, -448])
+
+
+def test_mixed_rows_roundtrip_error_bound():
+    v = rng.standard_normal((64, 576))
+    q = O.quantize_rows_e4m3(v, 512)
+    back = O.dequantize_rows_e4m3(q["codes"], q["scale"], q["rope"])
+    amax = np.abs(v[:, :512]).max(axis=1, keepdims=True)
+    # e4m3 has 3 mantissa bits: relative half-spacing 2^-4 in the normal range,
+    # absolute 2^-10 * scale in the subnormal range
+    err = np.abs(back[:, :512] - v[:, :512])
+    assert np.all(err <= np.maximum(np.abs(v[:, :512]) * 2.0 ** -4, amax / 448 * 2.0 ** -10) * 1.0001)
+    assert np.array_equal(back[:, 512:], O.round_to_bf16(v[:, 512:]))
+    # the largest element maps to the largest code 448 (or just below by scale rounding)
+    assert np.all(np.abs(O.decode_e4m3(q["codes"])).max(axis=1) >= 416)
+
+
+# ----------------------------------------------------------------- compress
+def test_compress_weights_sum_to_one_and_positive():
+    g = rng.standard_normal((64, 9))
+    b = 0.1 * rng.standard_normal((4, 9))
+    w = O.compress_weights(g, b, 4)
+    assert w.shape == (16, 4, 9)
+    assert np.all(w > 0)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+
+
+def test_compress_identical_tokens_give_that_token():
+    tok = rng.standard_normal(7)
+    x = np.tile(tok, (8, 1))
+    e = O.compress(x, rng.standard_normal((8, 7)), rng.standard_normal((4, 7)), 4)
+    np.testing.assert_allclose(e, np.tile(tok, (2, 1)), rtol=1e-15, atol=1e-15)
+
+
+def test_compress_m1_is_identity():
+    x = rng.standard_normal((5, 3))
+    assert np.array_equal(O.compress(x, rng.standard_normal((5, 3)), rng.standard_normal((1, 3)), 1), x)
+
+
+def test_compress_zero_gates_and_bias_is_block_mean():
+    x = rng.standard_normal((12, 5))
+    e = O.compress(x, np.zeros((12, 5)), np.zeros((4, 5)), 4)
+    np.testing.assert_allclose(e, x.reshape(3, 4, 5).mean(axis=1), rtol=1e-14, atol=1e-15)
+
+
+def test_compress_gate_shift_invariance():
+    x = rng.standard_normal((8, 6))
+    g = rng.standard_normal((8, 6))
+    b = rng.standard_normal((4, 6))
+    shift = np.repeat(rng.standard_normal((2, 6)) * 5, 4, axis=0)  # per (block, channel)
+    np.testing.assert_allclose(O.compress(x, g + shift, b, 4), O.compress(x, g, b, 4), rtol=1e-12,
+                               atol=1e-13)
+
+
+def test_compress_bias_selects_position_per_channel():
+    # a huge bias on position i of channel c makes the entry take token i there
+    m, C = 4, 6
+    x = rng.standard_normal((8, C))
+    bias = np.zeros((m, C))
+    pick = np.array([0, 3, 1, 2, 3, 0])
+    bias[pick, np.arange(C)] = 1000.0
+    e = O.compress(x, rng.standard_normal((8, C)), bias, m)
+    want = np.stack([x[blk * m + pick, np.arange(C)] for blk in range(2)])
+    np.testing.assert_allclose(e, want, rtol=0, atol=1e-300)
+
+
+def test_compress_drops_partial_tail():
+    assert O.compress(rng.standard_normal((11, 2)), rng.standard_normal((11, 2)), np.zeros((4, 2)), 4).shape == (2, 2)
+
+
+# ----------------------------------------------------------------- indexer
+def test_n_vis_matches_definition():
+    for m in (1, 4, 128):
+        for t in range(0, 600, 7):
+            brute = sum(1 for s in range(1000) if (s + 1) * m - 1 <= t)
+            assert O.n_vis(t, m) == brute
+
+
+def test_index_single_head_nonnegative_is_matmul():
+    q = np.abs(rng.standard_normal((6, 1, 16)))
+    k = np.abs(rng.standard_normal((10, 16)))
+    pos = np.arange(34, 40)  # m=4: n_vis = 8 .. 10
+    got = O.index_scores(q, np.ones((6, 1)), k, pos, 4)
+    ref = np.matmul(q[:, 0, :], k.T)
+    vis = np.arange(10)[None] < ((pos + 1) // 4)[:, None]
+    assert np.array_equal(np.isinf(got), ~vis)
+    np.testing.assert_allclose(got[vis], ref[vis], rtol=1e-14)
+
+
+def test_index_relu_clamps_negative_heads():
+    k = rng.standard_normal((4, 8))
+    q = np.stack([k[2], -k[2]])[None]  # head 0 aligned with key 2, head 1 opposite
+    got = O.index_scores(q, np.array([[0.3, 0.7]]), k, np.array([100]), 4)
+    assert got[0, 2] == pytest.approx(0.3 * float(k[2] @ k[2]), rel=1e-14)
+    # every key: head 1 contributes only where its dot product is positive
+    d0, d1 = q[0, 0] @ k.T, q[0, 1] @ k.T
+    np.testing.assert_allclose(got[0], 0.3 * np.maximum(d0, 0) + 0.7 * np.maximum(d1, 0), rtol=1e-14)
+
+
+def test_index_brute_force_tiny():
+    Q, H_I, d, N, m = 3, 3, 5, 7, 2
+    q = rng.standard_normal((Q, H_I, d))
+    w = rng.uniform(0, 1, (Q, H_I))
+    k = rng.standard_normal((N, d))
+    pos = np.array([3, 8, 13])
+    got = O.index_scores(q, w, k, pos, m)
+    for i in range(Q):
+        for s in range(N):
+            if (s + 1) * m - 1 <= pos[i]:
+                val = 0.0
+                for j in range(H_I):
+                    dot = sum(q[i, j, c] * k[s, c] for c in range(d))
+                    val += w[i, j] * max(0.0, dot)
+                assert got[i, s] == pytest.approx(val, rel=1e-13, abs=1e-14)
+            else:
+                assert got[i, s] == -math.inf
+
+
+def test_index_linear_in_w():
+    q = rng.standard_normal((4, 5, 8))
+    k = rng.standard_normal((9, 8))
+    w1, w2 = rng.uniform(0, 1, (4, 5)), rng.uniform(0, 1, (4, 5))
+    pos = np.full(4, 100)
+    np.testing.assert_allclose(O.index_scores(q, w1 + w2, k, pos, 4),
+                               O.index_scores(q, w1, k, pos, 4) + O.index_scores(q, w2, k, pos, 4),
+                               rtol=1e-13)
+
+
+# ----------------------------------------------------------------- top-k
+def test_topk_matches_stable_argsort():
+    for _ in range(200):
+        n = int(rng.integers(1, 300))
+        k = int(rng.integers(1, 64))
+        row = np.round(rng.standard_normal(n), int(rng.integers(0, 3)))  # plenty of ties
+        got = O.topk_row(row, n, k)
+        ref = np.sort(np.argsort(-row, kind="stable")[: min(k, n)])
+        assert np.array_equal(got, ref)
+
+
+def test_topk_brute_force_invariants_with_zero_ties():
+    for _ in range(300):
+        n = int(rng.integers(1, 12))
+        k = int(rng.integers(1, 8))
+        row = rng.choice([0.0, -0.0, 1.0, 2.0, -1.0], size=n)
+        sel = O.topk_row(row, n, k)
+        kk = min(k, n)
+        assert sel.size == kk and len(set(sel.tolist())) == kk
+        assert np.all(np.diff(sel) > 0) and np.all(sel < n)
+        uns = np.setdiff1d(np.arange(n), sel)
+        if uns.size and sel.size:
+            assert row[sel].min() >= row[uns].max()
+            tau = row[sel].min()
+            # ties at tau resolved to lower indices (signed zeros are equal)
+            tie_sel = sel[row[sel] == tau]
+            tie_uns = uns[row[uns] == tau]
+            if tie_uns.size:
+                assert tie_sel.max() < tie_uns.min()
+
+
+def test_topk_fewer_visible_than_k_pads():
+    scores = rng.standard_normal((3, 20))
+    pos = np.array([2, 9, 79])  # m=4: n_vis = 0, 2, 20
+    out = O.topk(scores, pos, 4, 5)
+    assert np.array_equal(out[0], [-1] * 5)
+    assert np.array_equal(out[1], [0, 1, -1, -1, -1])
+    assert np.array_equal(out[2], np.sort(np.argsort(-scores[2], kind="stable")[:5]))
+
+
+# ----------------------------------------------------------------- attention
+def _sdpa(q, k, v, scale, mask=None, causal=False):
+    # q [Q, H, D] -> [H, Q, D]; MQA: one k/v for every head
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(k)[None].expand(q.shape[1], -1, -1)
+    vt = torch.from_numpy(v)[None].expand(q.shape[1], -1, -1)
+    am = None if mask is None else torch.from_numpy(mask)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=am,
+                                                         is_causal=causal, scale=scale)
+    return o.permute(1, 0, 2).numpy()
+
+
+def _dense_case(T=24, H=3, D=10, D_v=7):
+    x = rng.standard_normal((T, D))
+    q = rng.standard_normal((T, H, D))
+    return x, q, D_v
+
+
+def test_csa_m1_allk_nowindow_is_dense_causal_mqa():
+    x, q, D_v = _dense_case()
+    T, D = x.shape
+    out, sel, _ = O.csa_pipeline(x=x, g=rng.standard_normal(x.shape), bias=np.zeros((1, D)),
+                                 xi=rng.standard_normal((T, 4)), gi=rng.standard_normal((T, 4)),
+                                 bias_i=np.zeros((1, 4)), q=q,
+                                 q_idx=rng.standard_normal((T, 2, 4)), w=rng.uniform(0, 1, (T, 2)),
+                                 m=1, k=T, W=0, D_v=D_v, scale=0.37, q_pos=np.arange(T),
+                                 kv_dtype="f64", key_dtype="f64")
+    ref = _sdpa(q, x, x[:, :D_v], 0.37, causal=True)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_hca_m1_nowindow_is_dense_causal_mqa():
+    x, q, D_v = _dense_case()
+    out = O.hca_attend(q, x, x, 0, np.arange(x.shape[0]), 1, 0, D_v, 0.21)
+    np.testing.assert_allclose(out, _sdpa(q, x, x[:, :D_v], 0.21, causal=True), rtol=1e-12,
+                               atol=1e-13)
+
+
+def test_window_keys_duplicate_entries_as_log2_bias():
+    # m = 1, all entries selected, window W: every window token is a key twice,
+    # which equals one copy with +log 2 on its logit
+    x, q, D_v = _dense_case(T=20)
+    T = x.shape[0]
+    W, scale = 5, 0.3
+    sel = [np.arange(t + 1) for t in range(T)]
+    out = O.csa_attend(q, x, x, 0, sel, np.arange(T), W, D_v, scale)
+    mask = np.full((T, T), -np.inf)
+    for t in range(T):
+        mask[t, : t + 1] = 0.0
+        mask[t, max(0, t - W + 1): t + 1] = math.log(2.0)
+    np.testing.assert_allclose(out, _sdpa(q, x, x[:, :D_v], scale, mask=mask), rtol=1e-12,
+                               atol=1e-13)
+
+
+def test_hca_window_and_blocks_brute_force():
+    # m = 4: query t sees entries s with 4s+3 <= t and raw tokens t-W+1..t
+    T, m, W, D, H = 23, 4, 3, 6, 2
+    e = rng.standard_normal((T // m, D))
+    raw = rng.standard_normal((T, D))
+    q = rng.standard_normal((T, H, D))
+    out = O.hca_attend(q, e, raw, 0, np.arange(T), m, W, 4, 0.5)
+    for t in (0, 2, 3, 7, 22):
+        keys = [e[s] for s in range(T // m) if 4 * s + 3 <= t] + [raw[u] for u in range(max(0, t - W + 1), t + 1)]
+        K = np.array(keys)
+        for h in range(H):
+            lg = np.array([0.5 * float(q[t, h] @ kk) for kk in K])
+            p = np.exp(lg - lg.max())
+            p /= p.sum()
+            np.testing.assert_allclose(out[t, h], p @ K[:, :4], rtol=1e-12, atol=1e-14)
+
+
+def test_attend_single_key_and_identical_keys_return_value():
+    k = rng.standard_normal((1, 9))
+    q = rng.standard_normal((4, 9))
+    np.testing.assert_allclose(O.attend_keys(q, k, 6, 1.0), np.tile(k[0, :6], (4, 1)), rtol=1e-15)
+    np.testing.assert_allclose(O.attend_keys(q, np.tile(k, (5, 1)), 6, 1.0), np.tile(k[0, :6], (4, 1)),
+                               rtol=1e-14)
+    assert np.array_equal(O.attend_keys(q, np.zeros((0, 9)), 6, 1.0), np.zeros((4, 6)))
+
+
+def test_attend_invariant_to_selection_order():
+    e = rng.standard_normal((30, 8))
+    q = rng.standard_normal((1, 3, 8))
+    sel = np.array([[3, 7, 11, 20, 29]])
+    a = O.csa_attend(q, e, e, 0, sel, np.array([200]), 0, 8, 0.4)
+    b = O.csa_attend(q, e, e, 0, sel[:, ::-1], np.array([200]), 0, 8, 0.4)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+
+
+def test_pipeline_selects_exactly_k_visible_entries():
+    T, m, k = 64, 4, 5
+    out, sel, scores = O.csa_pipeline(
+        x=rng.standard_normal((T, 8)), g=rng.standard_normal((T, 8)), bias=rng.standard_normal((m, 8)),
+        xi=rng.standard_normal((T, 4)), gi=rng.standard_normal((T, 4)), bias_i=rng.standard_normal((m, 4)),
+        q=rng.standard_normal((T, 2, 8)), q_idx=rng.standard_normal((T, 3, 4)), w=rng.uniform(0, 1, (T, 3)),
+        m=m, k=k, W=4, D_v=8, scale=0.3, q_pos=np.arange(T), kv_dtype="bf16", key_dtype="bf16")
+    for t in range(T):
+        nv = (t + 1) // m
+        s = sel[t][sel[t] >= 0]
+        assert s.size == min(k, nv)
+        assert np.all(s < nv)
