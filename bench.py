@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""CSA decode at 1M-token context on one B300: tokens/s, with the roofline
+fraction of the dominant kernel (the lightning-indexer stream over the
+compressed-key cache).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (default ``csa_decode_1m``): 32 sequences, one new token each at
+position 2^20 - 1, 262,144 compressed entries per sequence (576-wide bf16 KV
+entries, 128-wide bf16 indexer keys), 64 indexer heads, top-1024, 128 query
+heads sharing the KV, raw window 128.  A step is the whole CSA path for that
+token: compress the block the token completes (KV entry and indexer key),
+score all entries, keep the top 1024, attend over them plus the window.  The
+caches (12 GB) are resident; each step streams 2.2 GB, far more than the
+126 MB L2, so no L2 flush is needed between steps.
+
+With --gpus N > 1 (torchrun, one process per GPU) every rank runs its own
+32-sequence batch (replicas, weak scaling; no collective on the data path) and
+the time is the max over ranks.
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores over
+a bounded sample of the same workload: each step is the complete decode step
+of one sequence.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+METRIC = "CSA decode tok/s & prefill query-tok/s at 1M ctx; % of HBM/tensor roofline"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def _peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_decode_step(wl, inp, b):
+    """The oracle's complete decode step for sequence b (test infrastructure:
+    used here only for the timed CPU baseline)."""
+    import numpy as np
+    import oracle as O
+
+    def f64(t):
+        t = t.contiguous()
+        if t.dtype == torch.float32:
+            return t.double().numpy()
+        return O.decode_bf16(t.view(torch.int16).numpy().view(np.uint16))
+
+    N, m = wl.N, wl.m
+    x, g = f64(inp["x"][b]), f64(inp["g"][b])
+    xi, gi = f64(inp["xi"][b]), f64(inp["gi"][b])
+    kv = np.array(f64(inp["kv"][b]))
+    keys = np.array(f64(inp["keys"][b]))
+    a = (N - 1) * m - wl.raw_pos0
+    kv[N - 1] = O.store_rows(O.compress(x[a:a + m], g[a:a + m], f64(inp["bias"]), m), "bf16")
+    keys[N - 1] = O.store_rows(O.compress(xi[a:a + m], gi[a:a + m], f64(inp["bias_i"]), m), "bf16")
+    pos = np.array([wl.q_pos0])
+    scores = O.index_scores(f64(inp["q_idx"][b]), f64(inp["w"][b]), keys, pos, m)
+    sel = O.topk(scores, pos, m, wl.k)
+    return O.csa_attend(f64(inp["q"][b]), kv, x, wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)
+
+
+def _cpu_inputs(wl, nseq):
+    from long_context_sparse_25_b300 import synth
+    return synth.make_inputs(wl.replace(B=nseq), "cpu")
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = _cpu_inputs(wl, 1)
+    for _ in range(args.warmup):
+        _oracle_decode_step(wl, inp, 0)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_decode_step(wl, inp, 0)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = 1.0 / sec
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl),
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": "one sequence's complete decode step per timed step "
+                                   "(compress tail, index 262144 entries, top-1024, attend)"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def _config(wl):
+    return {"workload": f"{wl.name}: CSA decode, B={wl.B}, context {wl.L} tokens "
+                        f"({wl.N} entries), k={wl.k}, H={wl.H}, D={wl.D_v}+{wl.D_qk - wl.D_v}, "
+                        f"indexer {wl.H_I}x{wl.d_I}, window {wl.W}, bf16",
+            "B": wl.B, "context": wl.L, "entries": wl.N, "k": wl.k,
+            "l2": "inputs larger than L2 (2.2 GB streamed per step > 126 MB), no flush"}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = ROOT / "gpurun_out" / f"clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.path.parent.mkdir(exist_ok=True)
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            except Exception:
+                pass
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = [r.split(",") for r in self.path.read_text().strip().splitlines() if r.strip()]
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since those counters were taken."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text()).get(kernel)
+    if not d:
+        return None
+    src = ROOT / d["source"]
+    if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest()[:16] != d["sha"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+def run_ours(args, wl):
+    from long_context_sparse_25_b300 import csa, synth
+    from long_context_sparse_25_b300.pipeline import Step
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    stream = torch.cuda.Stream(device=dev)
+    p = step.p
+    N = wl.N
+    scores, sel = step.scores(), step.selected()
+    rest = step.ws[(sel.data_ptr() - step.ws.data_ptr()) + sel.numel() * 4:]
+    rest = rest[(256 - rest.data_ptr() % 256) % 256:]
+
+    # the step as its four C-ABI calls (the kernels csa_forward launches)
+    def calls():
+        return [
+            ("compress", lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, N - 1, N, step.kv,
+                                               x_pos0=wl.raw_pos0, stream=stream),
+                                  csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, N - 1, N,
+                                               step.keys, x_pos0=wl.raw_pos0, stream=stream))),
+            ("index", lambda: csa.index(p, inp["q_idx"], inp["w"], step.keys, wl.q_pos0, N, scores,
+                                        q_scale=inp.get("q_idx_scale"), stream=stream)),
+            ("topk", lambda: csa.topk(p, scores, wl.q_pos0, sel, ws=rest, stream=stream)),
+            ("attend", lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0,
+                                          N, step.out, ws=rest, stream=stream)),
+        ]
+
+    seq = calls()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for _, f in seq:
+                f()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)] for _ in range(args.steps)]
+    clocks = Clocks() if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            for j, (_, f) in enumerate(seq):
+                f()
+                ev[s][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = sum(ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps))
+    per_kernel = {name: sum(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)) / args.steps
+                  for j, (name, _) in enumerate(seq)}
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = wl.B * world / (ms / 1e3)
+
+    # end to end: the step's new inputs from pinned host memory, the output back
+    h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi")]
+    host_in = [t_.cpu().pin_memory() for t_ in h2d]
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    bi = sum(t_.numel() * t_.element_size() for t_ in h2d)
+    bo = host_out.numel() * host_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for d_, h_ in zip(h2d, host_in):
+                d_.copy_(h_, non_blocking=True)
+            step.run(stream=stream)
+            host_out.copy_(step.out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            for d_, h_ in zip(h2d, host_in):
+                d_.copy_(h_, non_blocking=True)
+            step.run(stream=stream)
+            host_out.copy_(step.out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    # roofline of the dominant kernel: the indexer's stream over the key cache
+    peak, peak_kind = _peaks()
+    idx_bytes = wl.B * (N * wl.d_I * 2 + wl.H_I * wl.d_I * 2 + wl.H_I * 4)
+    idx_ms = per_kernel["index"]
+    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        nseq = 2
+        cinp = _cpu_inputs(wl, nseq)
+        t0 = time.perf_counter()
+        for b in range(nseq):
+            _oracle_decode_step(wl, cinp, b)
+        sec = time.perf_counter() - t0
+        cpu = {"value": nseq / sec, "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"{nseq} of {wl.B} sequences, complete decode step each"}
+    launches_per_step = 2 + 1 + 1 + (2 if csa.workspace_size(p, csa.WS_ATTEND, 1, N) else 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(wl),
+        "roofline": {"bound": "hbm", "kernel": "index", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": _traffic("index_decode"),
+                     "algorithmic_bytes_per_launch": idx_bytes},
+        "per_kernel_ms": per_kernel,
+        "e2e": {"value": wl.B * world / (e2e_ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="csa_decode_1m")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from long_context_sparse_25_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,99 @@
+// Internal helpers shared by the kernels of libcsa_b300 (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+// ---------------------------------------------------------------- scalars
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(((uint32_t)h) << 16);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __nv_fp8_e4m3 v;
+  v.__x = c;
+  return (float)v;
+}
+
+// Load element `i` of a row stored as fp32 / bf16 (e4m3 rows go through
+// RowView below, which also applies the row scale).
+__device__ __forceinline__ float load_elem(const void* base, csa_dtype dt, int64_t i) {
+  if (dt == CSA_F32) return reinterpret_cast<const float*>(base)[i];
+  return bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[i]);
+}
+
+// Order-preserving map of an fp32 score to uint32: larger float -> larger key.
+// -0.0 is mapped like +0.0 so that signed zeros tie.
+__device__ __forceinline__ uint32_t score_key(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b << 1) == 0) b = 0;  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// A device view of one csa_rows block (passed by value into kernels).
+struct RowView {
+  csa_dtype dtype;
+  const void* data;
+  const uint16_t* rope;
+  const float* scale;
+  int64_t n_rows;
+  int width;
+  int nope;
+
+  __device__ __forceinline__ int64_t row_index(int b, int64_t r) const {
+    return (int64_t)b * n_rows + r;
+  }
+  // Channel c of row (b, r) as fp32 (e4m3 codes multiplied by the row scale).
+  __device__ __forceinline__ float get(int b, int64_t r, int c) const {
+    int64_t ri = row_index(b, r);
+    if (dtype == CSA_E4M3) {
+      if (c < nope)
+        return e4m3_to_f32(reinterpret_cast<const uint8_t*>(data)[ri * nope + c]) * scale[ri];
+      return bf16_to_f32(rope[ri * (width - nope) + (c - nope)]);
+    }
+    return load_elem(data, dtype, ri * width + c);
+  }
+};
+
+inline RowView make_view(const csa_rows& r) {
+  RowView v;
+  v.dtype = r.dtype;
+  v.data = r.data;
+  v.rope = reinterpret_cast<const uint16_t*>(r.rope);
+  v.scale = r.scale;
+  v.n_rows = r.n_rows;
+  v.width = r.width;
+  v.nope = r.dtype == CSA_E4M3 ? r.nope : r.width;
+  return v;
+}
+
+__host__ __device__ inline int64_t n_vis(int64_t t, int m) { return (t + 1) / m; }
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------- launchers (internal ABI)
+// Each returns cudaGetLastError() of its launches.
+cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype, const float* bias,
+                            int B, int64_t x_pos0, int64_t T, int m, int C, int64_t s_begin,
+                            int64_t s_end, const csa_rows& out, cudaStream_t st);
+
+cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
+                         const float* q_scale, const float* w, const csa_rows& keys,
+                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st);
+
+size_t topk_workspace(const csa_params& p, int Q, int64_t N);
+cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0, int Q, int64_t N,
+                        int32_t* idx, void* ws, cudaStream_t st);
+
+size_t attend_workspace(const csa_params& p, int Q, int64_t N, bool dense);
+cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype, const csa_rows& kv,
+                          const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                          int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
+                          void* ws, cudaStream_t st);
+
+}  // namespace csa

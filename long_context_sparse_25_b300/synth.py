@@ -1,0 +1,214 @@
+"""Seeded synthetic inputs for the CSA / HCA forward pass.
+
+This module only draws inputs: normal / uniform random numbers from a seeded
+torch generator (one generator per tensor, keyed on (seed, tensor id), so a
+tensor never depends on the size of another), the RMSNorm that the input
+recipe applies to query and KV rows, and the storage formats (bf16, or the
+mixed e4m3 + bf16 cache layout built with torch's own float8 cast).  It holds
+none of the method's arithmetic: no compression, scoring, selection or
+attention.  The same bytes feed the CUDA library and the CPU oracle.
+
+Workloads (sizes from the pages' configurations):
+
+* ``csa_tiny_f32``   -- CSA prefill, fp32, L=4096, m=4, indexer 4x64, k=64,
+  window 64, 16 heads x 128, K = V = entry.
+* ``csa_prefill_64k``-- CSA prefill, bf16, L=65536, indexer 64x128, k=1024,
+  128 heads, KV 512 + 64 rope dims, window 128.
+* ``csa_decode_1m``  -- CSA decode, bf16, B=32, context 1,048,576
+  (262,144 entries), k=1024, window 128.
+* ``hca_prefill_1m`` / ``hca_decode_1m`` -- HCA, m'=128 -> 8192 entries, an
+  8192-query tail chunk, and decode at B=32.
+* ``csa_decode_fp8_512k`` -- mixed-precision CSA decode, B=64, context
+  524,288: nope dims e4m3 + per-entry fp32 scale, rope dims bf16; indexer keys
+  and queries e4m3 with per-row scales; 1% of values x20.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from dataclasses import dataclass
+
+import torch
+
+RMS_EPS = 1e-6
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    mode: str          # "csa_prefill" | "csa_decode" | "hca_prefill" | "hca_decode"
+    B: int             # sequences
+    L: int             # tokens per sequence (the last query sits at L-1)
+    m: int             # block size (4 for CSA, 128 for HCA)
+    H: int
+    D_qk: int
+    D_v: int
+    H_I: int
+    d_I: int
+    k: int
+    W: int             # raw window
+    Q: int             # queries per sequence (tail chunk ending at L-1)
+    dtype: str         # "f32" | "bf16" | "mixed"
+    seed: int
+    rmsnorm: bool = True
+    outliers: float = 0.0   # probability that an element is multiplied by 20
+    q_std: float = 1.0      # extra factor on Q (the tiny case folds 1/sqrt(128))
+    softmax_scale: float | None = None
+
+    @property
+    def N(self) -> int:
+        """Entries per sequence."""
+        return self.L // self.m
+
+    @property
+    def scale(self) -> float:
+        return self.softmax_scale if self.softmax_scale is not None else 1.0 / math.sqrt(self.D_qk)
+
+    @property
+    def q_pos0(self) -> int:
+        return self.L - self.Q
+
+    @property
+    def raw_rows(self) -> int:
+        """Raw rows held in memory: all L for prefill, the window (which also
+        covers the block completed by the decode token) for decode."""
+        return self.L if self.mode.endswith("prefill") else max(self.W, self.m)
+
+    @property
+    def raw_pos0(self) -> int:
+        return self.L - self.raw_rows
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "csa_tiny_f32": Workload("csa_tiny_f32", "csa_prefill", B=1, L=4096, m=4, H=16, D_qk=128,
+                             D_v=128, H_I=4, d_I=64, k=64, W=64, Q=4096, dtype="f32", seed=0,
+                             rmsnorm=False, q_std=1.0 / math.sqrt(128), softmax_scale=1.0),
+    "csa_prefill_64k": Workload("csa_prefill_64k", "csa_prefill", B=1, L=65536, m=4, H=128,
+                                D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=65536,
+                                dtype="bf16", seed=1),
+    "csa_decode_1m": Workload("csa_decode_1m", "csa_decode", B=32, L=1 << 20, m=4, H=128,
+                              D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
+                              dtype="bf16", seed=2),
+    "hca_prefill_1m": Workload("hca_prefill_1m", "hca_prefill", B=1, L=1 << 20, m=128, H=128,
+                               D_qk=576, D_v=512, H_I=0, d_I=0, k=0, W=128, Q=8192,
+                               dtype="bf16", seed=3),
+    "hca_decode_1m": Workload("hca_decode_1m", "hca_decode", B=32, L=1 << 20, m=128, H=128,
+                              D_qk=576, D_v=512, H_I=0, d_I=0, k=0, W=128, Q=1,
+                              dtype="bf16", seed=3),
+    "csa_decode_fp8_512k": Workload("csa_decode_fp8_512k", "csa_decode", B=64, L=1 << 19, m=4,
+                                    H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128,
+                                    Q=1, dtype="mixed", seed=4, outliers=0.01),
+}
+
+# tensor ids (the generator of tensor `name` is seeded with seed * 1000 + id)
+_IDS = {"x": 1, "g": 2, "bias": 3, "xi": 4, "gi": 5, "bias_i": 6, "q": 7, "q_idx": 8,
+        "w": 9, "kv": 10, "keys": 11, "outl_kv": 12, "outl_keys": 13, "outl_q_idx": 14,
+        "outl_x": 15, "outl_q": 16}
+
+
+def _gen(wl: Workload, name: str, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed * 1000 + _IDS[name])
+    return g
+
+
+def _normal(wl, name, shape, device, std=1.0, rms=False, outl=None, chunk_rows=1 << 16):
+    """float32 N(0, std^2) tensor, optionally RMSNorm'd per last-dim row and with
+    outliers; drawn in row chunks of a fixed size so that memory stays bounded."""
+    gen = _gen(wl, name, device)
+    gen_o = _gen(wl, outl, device) if (outl is not None and wl.outliers > 0) else None
+    out = torch.empty(shape, dtype=torch.float32, device=device)
+    flat = out.view(-1, shape[-1])
+    for r0 in range(0, flat.shape[0], chunk_rows):
+        r1 = min(flat.shape[0], r0 + chunk_rows)
+        v = torch.randn((r1 - r0, shape[-1]), generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            v.mul_(std)
+        if rms:
+            v.mul_(torch.rsqrt(v.pow(2).mean(dim=-1, keepdim=True) + RMS_EPS))
+        if gen_o is not None:
+            u = torch.rand((r1 - r0, shape[-1]), generator=gen_o, device=device)
+            v = torch.where(u < wl.outliers, v * 20.0, v)
+        flat[r0:r1] = v
+    return out
+
+
+def _uniform(wl, name, shape, device):
+    return torch.rand(shape, generator=_gen(wl, name, device), device=device, dtype=torch.float32)
+
+
+def _store(v: torch.Tensor, dtype: str) -> torch.Tensor:
+    if dtype == "f32":
+        return v
+    return v.to(torch.bfloat16)
+
+
+def quantize_e4m3_rows(v: torch.Tensor, nope: int):
+    """(codes e4m3 [.., nope], scale f32 [..], rope bf16 [.., rest] or None):
+    per-row scale amax/448 over the nope channels (1 for an all-zero row)."""
+    amax = v[..., :nope].abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).float()
+    codes = (v[..., :nope] / scale.unsqueeze(-1)).to(torch.float8_e4m3fn)
+    rope = v[..., nope:].to(torch.bfloat16).contiguous() if v.shape[-1] > nope else None
+    return codes.contiguous(), scale.contiguous(), rope
+
+
+def make_inputs(wl: Workload, device="cpu") -> dict:
+    """All inputs of one workload as torch tensors on ``device``.
+
+    Keys: x, g (raw KV rows and gate logits, [B, raw_rows, D_qk]); bias [m, D_qk];
+    xi, gi, bias_i (indexer-key rows, gates, bias); q [B, Q, H, D_qk];
+    q_idx [B, Q, H_I, d_I] (+ q_idx_scale [B, Q, H_I] for mixed); w [B, Q, H_I];
+    for decode also the caches kv [B, N, D_qk] (or kv_nope / kv_rope / kv_scale)
+    and keys [B, N, d_I] (or keys + keys_scale), holding entries 0 .. N-2; the
+    decode step compresses entry N-1 from the raw rows.
+    """
+    B, R = wl.B, wl.raw_rows
+    rows_dtype = "f32" if wl.dtype == "f32" else "bf16"
+    inp = {}
+    inp["x"] = _store(_normal(wl, "x", (B, R, wl.D_qk), device, rms=wl.rmsnorm), rows_dtype)
+    inp["g"] = _store(_normal(wl, "g", (B, R, wl.D_qk), device), rows_dtype)
+    inp["bias"] = _normal(wl, "bias", (wl.m, wl.D_qk), device, std=0.1)
+    inp["q"] = _store(_normal(wl, "q", (B, wl.Q, wl.H, wl.D_qk), device, std=wl.q_std,
+                              rms=wl.rmsnorm, outl="outl_q"), rows_dtype)
+    if wl.mode.startswith("csa"):
+        inp["xi"] = _store(_normal(wl, "xi", (B, R, wl.d_I), device, rms=wl.rmsnorm), rows_dtype)
+        inp["gi"] = _store(_normal(wl, "gi", (B, R, wl.d_I), device), rows_dtype)
+        inp["bias_i"] = _normal(wl, "bias_i", (wl.m, wl.d_I), device, std=0.1)
+        qi = _normal(wl, "q_idx", (B, wl.Q, wl.H_I, wl.d_I), device, rms=wl.rmsnorm,
+                     outl="outl_q_idx")
+        if wl.dtype == "mixed":
+            codes, scale, _ = quantize_e4m3_rows(qi, wl.d_I)
+            inp["q_idx"], inp["q_idx_scale"] = codes, scale
+        else:
+            inp["q_idx"] = _store(qi, rows_dtype)
+        inp["w"] = _uniform(wl, "w", (B, wl.Q, wl.H_I), device)
+    if wl.mode.endswith("decode"):
+        N = wl.N
+        kv = _normal(wl, "kv", (B, N, wl.D_qk), device, rms=wl.rmsnorm, outl="outl_kv")
+        kv[:, N - 1].zero_()  # computed by the decode step
+        if wl.dtype == "mixed":
+            codes, scale, rope = quantize_e4m3_rows(kv, wl.D_v)
+            inp["kv_nope"], inp["kv_scale"], inp["kv_rope"] = codes, scale, rope
+        else:
+            inp["kv"] = _store(kv, rows_dtype)
+        del kv
+        if wl.mode.startswith("csa"):
+            keys = _normal(wl, "keys", (B, N, wl.d_I), device, rms=wl.rmsnorm, outl="outl_keys")
+            keys[:, N - 1].zero_()
+            if wl.dtype == "mixed":
+                codes, scale, _ = quantize_e4m3_rows(keys, wl.d_I)
+                inp["keys"], inp["keys_scale"] = codes, scale
+            else:
+                inp["keys"] = _store(keys, rows_dtype)
+    return inp
+
+
+def small(wl: Workload, **kw) -> Workload:
+    """A reduced copy of a workload (same recipe and dtypes, smaller sizes)."""
+    return wl.replace(**kw)

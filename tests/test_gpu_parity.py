@@ -1,0 +1,165 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs.
+
+Sizes the oracle finishes in seconds that still span several tiles and a
+ragged tail; the full-size workloads sit in test_gpu_fullsize.py."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from long_context_sparse_25_b300 import csa, synth
+from long_context_sparse_25_b300.pipeline import Step
+
+from harness import (SeqOracle, check_out, check_scores, check_selection, f64)
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+CSA_CASES = {
+    # fp32 tiny workload at its full size: every query
+    "tiny_f32": (W["csa_tiny_f32"], None),
+    # bf16 prefill, ragged length (2051 tokens -> 512 entries + 3-token tail)
+    "prefill_bf16_ragged": (W["csa_prefill_64k"].replace(L=2051, Q=2051, k=32), 160),
+    # bf16 prefill with the real k=1024 and more entries than k
+    "prefill_bf16_8k": (W["csa_prefill_64k"].replace(L=8192, Q=8192), 48),
+    # bf16 decode, 5000 entries (ragged w.r.t. 128-key tiles), batch 3
+    "decode_bf16": (W["csa_decode_1m"].replace(B=3, L=20000), None),
+    # mixed e4m3 + bf16 decode, 5001 entries
+    "decode_mixed": (W["csa_decode_fp8_512k"].replace(B=2, L=20004), None),
+}
+
+
+def _query_sample(wl, n):
+    if n is None or n >= wl.Q:
+        return np.arange(wl.Q)
+    rng = np.random.default_rng(wl.seed + 17)
+    head = np.arange(min(8, wl.Q))
+    tail = np.arange(max(0, wl.Q - 8), wl.Q)
+    mid = rng.choice(wl.Q, size=n, replace=False)
+    return np.unique(np.concatenate([head, mid, tail]))
+
+
+def _run(wl, dev):
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    return inp, step
+
+
+@pytest.mark.parametrize("case", list(CSA_CASES))
+def test_csa_forward_matches_oracle(case, cuda_device):
+    wl, nsample = CSA_CASES[case]
+    inp, step = _run(wl, cuda_device)
+    qs = _query_sample(wl, nsample)
+    out = f64(step.out)
+    sel = step.selected().cpu().numpy()
+    scores = step.scores().cpu().double().numpy()
+    decode = wl.mode.endswith("decode")
+    for b in range(wl.B):
+        o = SeqOracle(wl, inp, b)
+        # step 1: compressed entries and indexer keys (new rows only)
+        n0 = wl.N - 1 if decode else 0
+        if wl.dtype == "mixed":
+            got_kv = O.dequantize_rows_e4m3(inp["kv_nope"][b, n0:].cpu().view(torch.uint8).numpy(),
+                                            inp["kv_scale"][b, n0:].cpu().numpy(),
+                                            inp["kv_rope"][b, n0:].cpu().view(torch.int16).numpy().view(np.uint16))
+            got_keys = O.dequantize_rows_e4m3(inp["keys"][b, n0:].cpu().view(torch.uint8).numpy(),
+                                              inp["keys_scale"][b, n0:].cpu().numpy())
+        else:
+            kvt = inp["kv"] if decode else step.kv_buf
+            kt = inp["keys"] if decode else step.keys_buf
+            got_kv, got_keys = f64(kvt[b, n0:]), f64(kt[b, n0:])
+        if wl.dtype == "f32":
+            np.testing.assert_allclose(got_kv, o.new_kv, rtol=2e-6, atol=2e-6)
+            np.testing.assert_allclose(got_keys, o.new_keys, rtol=2e-6, atol=2e-6)
+        else:
+            # bf16 nearest to the exact value / e4m3 decided in float64: identical
+            assert np.array_equal(got_keys, o.new_keys), "indexer keys differ from the oracle"
+            assert np.array_equal(got_kv, o.new_kv), "entries differ from the oracle"
+        # step 2: scores; step 3: selection; step 4: attention on the GPU's set
+        ref_scores = o.scores(qs)
+        check_scores(scores[b, qs], ref_scores)
+        check_selection(sel[b, qs], ref_scores, O.n_vis(o.positions(qs), wl.m), wl.k)
+        ref_out = o.attend(qs, sel[b, qs])
+        check_out(out[b, qs], ref_out, wl.dtype == "f32")
+
+
+HCA_CASES = {
+    "hca_prefill_ragged": W["hca_prefill_1m"].replace(L=128 * 100 + 57, Q=300),
+    "hca_decode": W["hca_decode_1m"].replace(B=3, L=128 * 300),
+}
+
+
+@pytest.mark.parametrize("case", list(HCA_CASES))
+def test_hca_matches_oracle(case, cuda_device):
+    wl = HCA_CASES[case]
+    inp, step = _run(wl, cuda_device)
+    out = f64(step.out)
+    decode = wl.mode.endswith("decode")
+    n0 = wl.N - 1 if decode else 0
+    for b in range(wl.B):
+        o = SeqOracle(wl, inp, b)
+        got_kv = f64((inp["kv"] if decode else step.kv_buf)[b, n0:])
+        # m' = 128 > 16: fp32 pooling rounded once to bf16 -> within one bf16 step
+        np.testing.assert_allclose(got_kv, o.new_kv, rtol=2 ** -8, atol=1e-6)
+        qs = np.arange(wl.Q)
+        check_out(out[b], o.hca(qs), False)
+
+
+def test_topk_bit_exact_on_oracle_scores(cuda_device):
+    """csa_topk fed fp32 scores (with many exact ties, signed zeros, -inf
+    beyond visibility) returns exactly the oracle's index lists."""
+    rng = np.random.default_rng(5)
+    for (B, Q, N, k, m, q_pos0) in [(2, 37, 700, 64, 4, 2700), (1, 5, 20000, 1024, 4, 79999),
+                                     (3, 9, 300, 1024, 4, 1000), (1, 300, 16384, 1024, 4, 65235)]:
+        s = rng.standard_normal((B, Q, N))
+        s = np.where(rng.uniform(size=s.shape) < 0.3, np.round(s, 1), s)  # ties
+        s = np.where(rng.uniform(size=s.shape) < 0.05, 0.0, s)
+        s = np.where(rng.uniform(size=s.shape) < 0.05, -0.0, s)
+        s[0, 0, :] = 1.5  # one row of all-equal scores
+        s32 = s.astype(np.float32)
+        pos = q_pos0 + np.arange(Q)
+        nv = O.n_vis(pos, m)
+        s32 = np.where(np.arange(N)[None, None] < nv[None, :, None], s32, -np.inf).astype(np.float32)
+        p = csa.params(B, m, k=k)
+        idx = torch.empty((B, Q, k), dtype=torch.int32, device=cuda_device)
+        csa.topk(p, torch.from_numpy(s32).to(cuda_device), q_pos0, idx)
+        got = idx.cpu().numpy()
+        for b in range(B):
+            ref = O.topk(s32[b].astype(np.float64), pos, m, k)
+            assert np.array_equal(got[b], ref)
+
+
+def test_batch_invariance_and_determinism(cuda_device):
+    """A sequence gives bitwise the same output alone or at any batch slot,
+    and two runs give bitwise the same output."""
+    wl = W["csa_decode_1m"].replace(B=4, L=12000)
+    inp, step = _run(wl, cuda_device)
+    first = step.out.clone()
+    step.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first, step.out)
+    for b in (0, 2):
+        one = {k: (v if k in ("bias", "bias_i") else v[b: b + 1].contiguous()) for k, v in inp.items()}
+        s1 = Step(wl.replace(B=1), one)
+        s1.run()
+        torch.cuda.synchronize()
+        assert torch.equal(s1.out[0], first[b]), f"sequence {b} differs alone"
+
+
+def test_empty_and_degenerate_cases(cuda_device):
+    """Queries that see no entry (t < m-1) and W = 0 give zeros; Q = 0 and
+    N = 0 launch nothing and succeed."""
+    wl = W["csa_tiny_f32"].replace(L=16, Q=16, W=0, k=4)
+    inp, step = _run(wl, cuda_device)
+    out = step.out.cpu()
+    assert torch.count_nonzero(out[0, :3]) == 0  # positions 0..2: no visible entry, no window
+    o = SeqOracle(wl, inp, 0)
+    qs = np.arange(wl.Q)
+    check_out(f64(step.out[0]), o.attend(qs, step.selected()[0].cpu().numpy()), True)
+    p = csa.params(1, 4, 16, 128, 128, 4, 64, 4, 0, 1.0)
+    empty = torch.empty((1, 0, 4, 64), device=cuda_device)
+    csa.index(p, empty, torch.empty((1, 0, 4), device=cuda_device), csa.rows(inp["xi"]), 0, 0,
+              torch.empty((1, 0, 0), device=cuda_device))
