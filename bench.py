@@ -220,31 +220,53 @@ def run_ours(args, wl):
     p = step.p
     N = wl.N
     scores, sel = step.scores(), step.selected()
-    rest = step.ws[(sel.data_ptr() - step.ws.data_ptr()) + sel.numel() * 4:]
-    rest = rest[(256 - rest.data_ptr() % 256) % 256:]
+    off = sel.data_ptr() - step.ws.data_ptr() + sel.numel() * 4
+    off = (off + 255) // 256 * 256
+    rest = step.ws[off:]
 
-    # the step as its four C-ABI calls (the kernels csa_forward launches)
-    def calls():
-        return [
-            ("compress", lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, N - 1, N, step.kv,
-                                               x_pos0=wl.raw_pos0, stream=stream),
-                                  csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, N - 1, N,
-                                               step.keys, x_pos0=wl.raw_pos0, stream=stream))),
-            ("index", lambda: csa.index(p, inp["q_idx"], inp["w"], step.keys, wl.q_pos0, N, scores,
-                                        q_scale=inp.get("q_idx_scale"), stream=stream)),
-            ("topk", lambda: csa.topk(p, scores, wl.q_pos0, sel, ws=rest, stream=stream)),
-            ("attend", lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0,
-                                          N, step.out, ws=rest, stream=stream)),
-        ]
-
-    seq = calls()
+    # the step's C-ABI calls one by one (the kernels csa_forward launches),
+    # used to time each part in a graph of its own
+    parts = {
+        "compress": lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, N - 1, N, step.kv,
+                                          x_pos0=wl.raw_pos0, stream=stream),
+                             csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, N - 1, N,
+                                          step.keys, x_pos0=wl.raw_pos0, stream=stream)),
+        "index": lambda: csa.index(p, inp["q_idx"], inp["w"], step.keys, wl.q_pos0, N, scores,
+                                   q_scale=inp.get("q_idx_scale"), stream=stream),
+        "topk": lambda: csa.topk(p, scores, wl.q_pos0, sel, ws=rest, stream=stream),
+        "attend": lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0,
+                                     N, step.out, ws=rest, stream=stream),
+    }
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            for _, f in seq:
+        for _ in range(2):
+            step.run(stream=stream)
+            for f in parts.values():
                 f()
     torch.cuda.synchronize()
+    csa.device_status(stream)
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        step.run(stream=stream)
+    g_part = {}
+    for name, f in parts.items():
+        g_part[name] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_part[name], stream=stream):
+            f()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_full.replay()
+    torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)] for _ in range(args.steps)]
+    def timed(graph, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for a_, b_ in evs:
+                a_.record(stream)
+                graph.replay()
+                b_.record(stream)
+        return evs
+
     clocks = Clocks() if rank == 0 else None
     if dist:
         dist.barrier()
@@ -252,25 +274,27 @@ def run_ours(args, wl):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    with torch.cuda.stream(stream):
-        for s in range(args.steps):
-            ev[s][0].record(stream)
-            for j, (_, f) in enumerate(seq):
-                f()
-                ev[s][j + 1].record(stream)
+    ev = timed(g_full, args.steps)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    total_ms = sum(ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps))
-    per_kernel = {name: sum(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)) / args.steps
-                  for j, (name, _) in enumerate(seq)}
+    total_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms = float(t.item())
     ms = total_ms / args.steps
     value = wl.B * world / (ms / 1e3)
+    csa.device_status(stream)
+
+    # each part on its own (same kernels, same data), for the roofline and
+    # the breakdown
+    per_kernel = {}
+    for name, g_ in g_part.items():
+        evs = timed(g_, args.steps)
+        torch.cuda.synchronize()
+        per_kernel[name] = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
 
     # end to end: the step's new inputs from pinned host memory, the output back
     h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi")]
@@ -280,17 +304,12 @@ def run_ours(args, wl):
     bo = host_out.numel() * host_out.element_size()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for _ in range(2):
+        for it in range(args.steps + 2):
+            if it == 2:
+                e0.record(stream)
             for d_, h_ in zip(h2d, host_in):
                 d_.copy_(h_, non_blocking=True)
-            step.run(stream=stream)
-            host_out.copy_(step.out, non_blocking=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            for d_, h_ in zip(h2d, host_in):
-                d_.copy_(h_, non_blocking=True)
-            step.run(stream=stream)
+            g_full.replay()
             host_out.copy_(step.out, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -320,7 +339,7 @@ def run_ours(args, wl):
         sec = time.perf_counter() - t0
         cpu = {"value": nseq / sec, "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{nseq} of {wl.B} sequences, complete decode step each"}
-    launches_per_step = 2 + 1 + 1 + (2 if csa.workspace_size(p, csa.WS_ATTEND, 1, N) else 1)
+    launches_per_step = step.launches_per_step()
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -329,7 +348,9 @@ def run_ours(args, wl):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _traffic("index_decode"),
                      "algorithmic_bytes_per_launch": idx_bytes},
-        "per_kernel_ms": per_kernel,
+        "per_part_ms": per_kernel,
+        "timing": "CUDA graph of the whole step replayed per timed step; CUDA events on the "
+                  "launching stream; the indexer timed alone in its own graph for the roofline",
         "e2e": {"value": wl.B * world / (e2e_ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": launches_per_step * args.steps,

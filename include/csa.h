@@ -244,6 +244,16 @@ enum { CSA_WS_TOPK = 0, CSA_WS_ATTEND = 1, CSA_WS_HCA = 2, CSA_WS_FORWARD = 3 };
  * sequence over N entries; 0 on invalid arguments. */
 size_t csa_workspace_size(const csa_params* p, int which, int Q, int64_t N);
 
+/*
+ * csa_device_status -- synchronise `stream` and report whether a bounded
+ * device-side wait in a kernel launched since the previous check gave up
+ * (CSA_ERR_TIMEOUT; the outputs of those calls are then not valid).  The
+ * tensor-core kernels wait on mbarriers for their own TMA copies and MMAs;
+ * each wait gives up after 2 s instead of hanging, records the site and lets
+ * the kernel exit.  Clears the recorded state.  CSA_OK otherwise.
+ */
+int csa_device_status(csa_stream_t stream);
+
 /* Message describing the last error returned on the calling thread ("" if none). */
 const char* csa_last_error(void);
 

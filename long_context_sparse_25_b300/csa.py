@@ -79,6 +79,8 @@ for _name, _args in _SIGS.items():
     _f.restype = C.c_int
 lib.csa_workspace_size.argtypes = [C.POINTER(Params), _I, _I, _I64]
 lib.csa_workspace_size.restype = C.c_size_t
+lib.csa_device_status.argtypes = [_P]
+lib.csa_device_status.restype = C.c_int
 lib.csa_last_error.argtypes = []
 lib.csa_last_error.restype = C.c_char_p
 
@@ -135,6 +137,11 @@ def workspace_size(p: Params, which: int, Q: int, N: int) -> int:
     return int(lib.csa_workspace_size(C.byref(p), which, Q, N))
 
 
+def topk_launches(p: Params, Q: int, N: int) -> int:
+    """Kernels one csa_topk call launches for these sizes."""
+    return 1
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
     if nbytes == 0:
         return None
@@ -189,6 +196,12 @@ def forward_args(*, x, gate, bias, xi, gate_i, bias_i, raw_pos0, q, q_idx, w, q_
                        dtype_code(x), x.shape[1], raw_pos0, _ptr(q), dtype_code(q), _ptr(q_idx),
                        dtype_code(q_idx), _ptr(q_idx_scale), _ptr(w), q_pos0, q.shape[1], kv, keys,
                        n_cached, _ptr(out), dtype_code(out))
+
+
+def device_status(stream=None):
+    """Synchronise the stream; raise CsaError(CSA_ERR_TIMEOUT) if a bounded
+    device-side wait gave up since the previous check."""
+    _check(lib.csa_device_status(_stream(stream)))
 
 
 def forward(p: Params, a: ForwardArgs, ws: torch.Tensor, stream=None):

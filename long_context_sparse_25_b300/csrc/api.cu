@@ -134,6 +134,16 @@ extern "C" {
 
 const char* csa_last_error(void) { return g_err; }
 
+int csa_device_status(csa_stream_t stream) {
+  int code = 0;
+  cudaError_t e = index_tc_status(&code, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "csa_device_status");
+  if (code != 0)
+    return fail(CSA_ERR_TIMEOUT, "a bounded device-side wait gave up (site %d); the outputs of the "
+                                 "calls since the last check are not valid", code);
+  return ok();
+}
+
 int csa_compress(const void* x, const void* gate, csa_dtype in_dtype, const float* bias, int B,
                  int64_t x_pos0, int64_t T, int m, int C, int64_t s_begin, int64_t s_end,
                  const csa_rows* out, csa_stream_t stream) {
@@ -330,7 +340,7 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
     if (e != cudaSuccess) return cuda_status(e, "csa_forward/compress keys");
   }
   e = launch_index(*p, a->q_idx, a->q_idx_dtype, a->q_idx_scale, a->w, a->keys, a->q_pos0, a->Q, N,
-                   scores, st);
+                   scores, st, /*fill_invisible=*/false);
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/index");
   e = launch_topk(*p, scores, a->q_pos0, a->Q, N, idx, rest, st);
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/topk");

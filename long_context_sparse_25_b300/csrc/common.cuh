@@ -82,11 +82,18 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
                             int B, int64_t x_pos0, int64_t T, int m, int C, int64_t s_begin,
                             int64_t s_end, const csa_rows& out, cudaStream_t st);
 
+// fill_invisible: write -inf for entries beyond each query's visibility (the
+// fused forward skips it: top-k never reads them).
 cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                          const float* q_scale, const float* w, const csa_rows& keys,
-                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st);
+                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
+                         bool fill_invisible = true);
+
+// Reads and clears the device error word of the bounded waits (0 = none).
+cudaError_t index_tc_status(int* code, cudaStream_t st);
 
 size_t topk_workspace(const csa_params& p, int Q, int64_t N);
+int topk_launches(const csa_params& p, int Q, int64_t N);
 cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0, int Q, int64_t N,
                         int32_t* idx, void* ws, cudaStream_t st);
 

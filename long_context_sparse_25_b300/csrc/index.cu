@@ -18,7 +18,8 @@ namespace csa {
 bool index_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& keys, int Q);
 cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                             const float* q_scale, const float* w, const csa_rows& keys,
-                            int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st);
+                            int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
+                            bool fill_invisible);
 
 namespace {
 
@@ -70,10 +71,12 @@ __global__ void __launch_bounds__(kKeysPerCta) index_simt_kernel(
 
 cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                          const float* q_scale, const float* w, const csa_rows& keys,
-                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st) {
+                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
+                         bool fill_invisible) {
   if (N <= 0 || Q <= 0 || p.B <= 0) return cudaSuccess;
   if (index_tc_supported(p, q_dtype, keys, Q))
-    return launch_index_tc(p, q_idx, q_dtype, q_scale, w, keys, q_pos0, Q, N, scores, st);
+    return launch_index_tc(p, q_idx, q_dtype, q_scale, w, keys, q_pos0, Q, N, scores, st,
+                           fill_invisible);
   const int64_t blocks = ceil_div(N, kKeysPerCta) * Q * p.B;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)blocks);

@@ -1,16 +1,457 @@
-// Tensor-core (tcgen05 / TMEM / TMA) path of the lightning indexer.
+// Tensor-core path of the lightning indexer (tcgen05 MMA, TMEM accumulators,
+// TMA-fed shared-memory ring).
+//
+//   I[b,i,s] = sum_j w[b,i,j] * max(0, q_idx[b,i,j,:] . keys[b,s,:])
+//
+// Sources: "一文搞懂 DeepSeek：从 V3 的 KV 压缩与 MoE，到 V4 的百万 token 上下文",
+// section "V4 改进一：CSA 与 HCA" (the lightning indexer scores every compressed
+// entry); "DeepSeek-V4 详解" section 2.2 Step 2 (DSA-style indexer in FP8).
+//
+// Mapping.  One MMA tile is D[128 keys x NQ*H_I] = K_tile[128 x d_I] .
+// Qblk[NQ*H_I x d_I]^T: the keys are the M side, so that each TMEM lane (one
+// thread of the epilogue) holds every head of its key and the head reduction
+// sum_j w_j ReLU(.) stays inside one thread.  Decode (one query per sequence)
+// uses N = 64 and streams the key cache from HBM; prefill packs NQ = 4 queries
+// (N = 256) so that each key tile read from L2 feeds 4x more MMA work.
+//
+// Roles (warp-specialised, one CTA per SM, persistent):
+//   warp 0      TMA producer: key tiles into a ring of stages, query blocks
+//               into one or two B buffers;
+//   warp 1      TMEM allocator and MMA issuer (one thread);
+//   warps 2..   epilogue: tcgen05.ld of the accumulator, ReLU, weighted head
+//               sum, e4m3 row scales, coalesced fp32 stores of the scores.
+// Accumulators are double-buffered in TMEM so the epilogue of tile t overlaps
+// the MMA of tile t+1.  Every mbarrier wait is bounded; a timeout is recorded
+// in a device error word (read by csa_device_status) and the kernel returns.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace csa {
 
-bool index_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& keys, int Q) {
-  (void)p; (void)q_dtype; (void)keys; (void)Q;
-  return false;
+namespace {
+
+__device__ int g_index_tc_error = 0;
+
+constexpr int kTileKeys = 128;
+
+struct TcArgs {
+  int B, Q, H_I, d_I, m, NQ, nQB, tps;  // tps: key tiles per sequence (all N)
+  int64_t N, n_rows, q_pos0;
+  int mode;                             // 0: every query block sees all tiles; 1: causal units
+  int64_t total;                        // mode 0: B*nQB*tps tiles; mode 1: B*nQB units
+  int stages, nb;
+  uint32_t a_bytes, b_bytes, a_chunk_bytes, b_chunk_bytes;
+  int chunk_elems, n_chunks, ksteps;
+  uint32_t tmem_cols;
+  const float* w;
+  const float* q_scale;  // e4m3 only
+  const float* k_scale;  // e4m3 only
+  float* scores;
+};
+
+__device__ __forceinline__ int tiles_visible(const TcArgs& a, int qb) {
+  int last = (qb + 1) * a.NQ;
+  if (last > a.Q) last = a.Q;
+  int64_t nv = n_vis(a.q_pos0 + last - 1, a.m);
+  if (nv > a.N) nv = a.N;
+  return (int)((nv + kTileKeys - 1) / kTileKeys);
 }
 
-cudaError_t launch_index_tc(const csa_params&, const void*, csa_dtype, const float*, const float*,
-                            const csa_rows&, int64_t, int, int64_t, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
+// The (b, qb, kt) tiles of one CTA, in the same order for every role.
+struct Sched {
+  const TcArgs* a;
+  int c, G;
+  int64_t t, t_end;  // mode 0
+  int64_t r;         // mode 1: round
+  int b, qb, kt, kt_end;
+
+  __device__ void init(const TcArgs& args, int cta, int grid) {
+    a = &args;
+    c = cta;
+    G = grid;
+    if (args.mode == 0) {
+      t = args.total * cta / grid;
+      t_end = args.total * (cta + 1) / grid;
+    } else {
+      r = 0;
+      kt = 0;
+      kt_end = 0;
+    }
+  }
+
+  __device__ bool next(int& ob, int& oqb, int& okt) {
+    if (a->mode == 0) {
+      if (t >= t_end) return false;
+      const int64_t per_b = (int64_t)a->nQB * a->tps;
+      ob = (int)(t / per_b);
+      oqb = (int)((t / a->tps) % a->nQB);
+      okt = (int)(t % a->tps);
+      ++t;
+      return true;
+    }
+    while (kt >= kt_end) {
+      // zig-zag over units ordered from the heaviest (latest queries) down
+      int64_t p = r * G + ((r & 1) ? (G - 1 - c) : c);
+      ++r;
+      if (p >= a->total) return false;
+      int64_t u = a->total - 1 - p;
+      qb = (int)(u / a->B);
+      b = (int)(u % a->B);
+      kt = 0;
+      kt_end = tiles_visible(*a, qb);
+    }
+    ob = b;
+    oqb = qb;
+    okt = kt++;
+    return true;
+  }
+};
+
+template <bool kFP8, int kEpiWG>
+__global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
+    index_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
+                    const __grid_constant__ CUtensorMap tm_q, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + (size_t)a.stages * a.a_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)a.nb * a.b_bytes);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = bars + a.stages;
+  uint64_t* b_full = bars + 2 * a.stages;
+  uint64_t* b_empty = b_full + 2;
+  uint64_t* acc_full = b_empty + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NM = a.NQ * a.H_I;  // MMA N
+  int* err = &g_index_tc_error;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&a_full[s], 1);
+      tc::mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&b_full[s], 1);
+      tc::mbar_init(&b_empty[s], 1);
+      tc::mbar_init(&acc_full[s], 1);
+      tc::mbar_init(&acc_empty[s], 4 * kEpiWG);
+    }
+    tc::mbar_init(mma_done, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tm_keys);
+    tc::prefetch_tmap(&tm_q);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, a.tmem_cols);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  Sched sch;
+  sch.init(a, blockIdx.x, gridDim.x);
+  int b, qb, kt;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t it = 0, qcount = 0;
+      int pb = -1, pqb = -1;
+      while (sch.next(b, qb, kt)) {
+        if (b != pb || qb != pqb) {
+          const uint32_t bi = qcount % a.nb;
+          if (!tc::mbar_wait(&b_empty[bi], ((qcount / a.nb) & 1) ^ 1, err, 1)) break;
+          tc::mbar_expect_tx(&b_full[bi], a.b_bytes);
+          const int y = (b * a.Q + qb * a.NQ) * a.H_I;
+          for (int ch = 0; ch < a.n_chunks; ++ch)
+            tc::tma_load_2d(sB + bi * a.b_bytes + ch * a.b_chunk_bytes, &tm_q, &b_full[bi],
+                            ch * a.chunk_elems, y);
+          ++qcount;
+          pb = b;
+          pqb = qb;
+        }
+        const uint32_t s = it % a.stages;
+        if (!tc::mbar_wait(&a_empty[s], ((it / a.stages) & 1) ^ 1, err, 2)) break;
+        tc::mbar_expect_tx(&a_full[s], a.a_bytes);
+        const int y = (int)((int64_t)b * a.n_rows + (int64_t)kt * kTileKeys);
+        for (int ch = 0; ch < a.n_chunks; ++ch)
+          tc::tma_load_2d(sA + s * a.a_bytes + ch * a.a_chunk_bytes, &tm_keys, &a_full[s],
+                          ch * a.chunk_elems, y);
+        ++it;
+      }
+      // let the loads this CTA issued land before it can exit (only matters
+      // when a wait above gave up; otherwise the MMA issuer consumed them all)
+      for (uint32_t j = it > (uint32_t)a.stages ? it - a.stages : 0; j < it; ++j)
+        tc::mbar_drain(&a_full[j % a.stages], (j / a.stages) & 1);
+      for (uint32_t j = qcount > (uint32_t)a.nb ? qcount - a.nb : 0; j < qcount; ++j)
+        tc::mbar_drain(&b_full[j % a.nb], (j / a.nb) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t id = kFP8 ? tc::idesc(kTileKeys, NM, 0, 0) : tc::idesc(kTileKeys, NM, 1, 1);
+      const int kstep_bytes = 32;  // 16 bf16 or 32 e4m3 per MMA
+      const int steps_per_chunk = 128 / kstep_bytes;
+      uint32_t it = 0, qcount = 0, acc_it = 0, bi = 0;
+      int pb = -1, pqb = -1;
+      bool ok = true;
+      while (ok && sch.next(b, qb, kt)) {
+        if (b != pb || qb != pqb) {
+          if (qcount > 0) tc::mma_commit(&b_empty[(qcount - 1) % a.nb]);
+          bi = qcount % a.nb;
+          if (!tc::mbar_wait(&b_full[bi], (qcount / a.nb) & 1, err, 3)) { ok = false; break; }
+          ++qcount;
+          pb = b;
+          pqb = qb;
+        }
+        const uint32_t s = it % a.stages;
+        if (!tc::mbar_wait(&a_full[s], (it / a.stages) & 1, err, 4)) { ok = false; break; }
+        const uint32_t acc = acc_it & 1;
+        if (!tc::mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, err, 5)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + acc * NM;
+        const uint32_t a0 = tc::smem_u32(sA + s * a.a_bytes);
+        const uint32_t b0 = tc::smem_u32(sB + bi * a.b_bytes);
+        for (int kk = 0; kk < a.ksteps; ++kk) {
+          const int ch = kk / steps_per_chunk, off = (kk % steps_per_chunk) * kstep_bytes;
+          const uint64_t ad = tc::sdesc_sw128(a0 + ch * a.a_chunk_bytes + off);
+          const uint64_t bd = tc::sdesc_sw128(b0 + ch * a.b_chunk_bytes + off);
+          if (kFP8) tc::mma_e4m3(d, ad, bd, id, kk > 0);
+          else tc::mma_bf16(d, ad, bd, id, kk > 0);
+        }
+        tc::mma_commit(&a_empty[s]);
+        tc::mma_commit(&acc_full[acc]);
+        ++it;
+        ++acc_it;
+      }
+      // every MMA issued must have completed before TMEM is released
+      tc::mma_commit(mma_done);
+      tc::mbar_drain(mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int wg = ew >> 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    const int QPW = a.NQ / kEpiWG;  // queries per warpgroup
+    uint32_t acc_it = 0;
+    while (sch.next(b, qb, kt)) {
+      const uint32_t acc = acc_it & 1;
+      // one lane waits, the warp follows converged (tcgen05.ld is .sync.aligned)
+      int okw = lane == 0 ? (int)tc::mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, err, 6) : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      if (!okw) break;
+      tc::tc_fence_after();
+      float sc[4];
+      for (int ql = 0; ql < QPW; ++ql) {
+        const int qi = wg * QPW + ql;
+        const int i = qb * a.NQ + qi;
+        float acc_s = 0.f;
+        const uint32_t col = acc * NM + qi * a.H_I;
+        const int64_t wrow = ((int64_t)b * a.Q + (i < a.Q ? i : a.Q - 1)) * a.H_I;
+        for (int j0 = 0; j0 < a.H_I; j0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col + j0, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            float wj = __ldg(a.w + wrow + j0 + jj);
+            if (kFP8) wj *= __ldg(a.q_scale + wrow + j0 + jj);
+            acc_s = fmaf(wj, fmaxf(__uint_as_float(r[jj]), 0.f), acc_s);
+          }
+        }
+        sc[ql] = acc_s;
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
+      const int64_t s = (int64_t)kt * kTileKeys + row;
+      if (s < a.N) {
+        float ks = 1.f;
+        if (kFP8) ks = __ldg(a.k_scale + (int64_t)b * a.n_rows + s);
+        for (int ql = 0; ql < QPW; ++ql) {
+          const int i = qb * a.NQ + wg * QPW + ql;
+          if (i >= a.Q) break;
+          int64_t nv = n_vis(a.q_pos0 + i, a.m);
+          if (nv > a.N) nv = a.N;
+          a.scores[((int64_t)b * a.Q + i) * a.N + s] = s < nv ? sc[ql] * ks : -INFINITY;
+        }
+      }
+      ++acc_it;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+// -inf for entries beyond each query's visibility (the causal part of a
+// prefill score matrix that the tensor-core kernel never touches).
+__global__ void fill_invisible_kernel(float* __restrict__ scores, int Q, int64_t N, int m,
+                                      int64_t q_pos0) {
+  const int64_t row = blockIdx.x;  // b * Q + i
+  const int i = (int)(row % Q);
+  const int64_t nv = n_vis(q_pos0 + i, m);
+  for (int64_t s = nv + threadIdx.x; s < N; s += blockDim.x) scores[row * N + s] = -INFINITY;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of 1- or 2-byte elements with a
+// box of 128 bytes x box_rows and the 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, bool fp8, int64_t rows, int cols, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+bool index_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& keys, int Q) {
+  (void)Q;
+  const bool fp8 = keys.dtype == CSA_E4M3;
+  if (fp8 != (q_dtype == CSA_E4M3)) return false;
+  if (!fp8 && !(keys.dtype == CSA_BF16 && q_dtype == CSA_BF16)) return false;
+  if (fp8 && keys.nope != keys.width) return false;
+  const int esz = fp8 ? 1 : 2;
+  if ((p.d_I * esz) % 128 != 0 || p.d_I * esz > 512) return false;
+  if (p.H_I % 32 != 0 || p.H_I > 256) return false;
+  if ((int64_t)p.B * keys.n_rows >= (1ll << 31)) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t index_tc_status(int* code, cudaStream_t st) {
+  int h = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_index_tc_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  *code = h;
+  if (h != 0) {
+    int zero = 0;
+    e = cudaMemcpyToSymbol(g_index_tc_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
+                            const float* q_scale, const float* w, const csa_rows& keys,
+                            int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
+                            bool fill_invisible) {
+  const bool fp8 = keys.dtype == CSA_E4M3;
+  (void)q_dtype;
+  TcArgs a{};
+  a.B = p.B;
+  a.Q = Q;
+  a.H_I = p.H_I;
+  a.d_I = p.d_I;
+  a.m = p.m;
+  a.N = N;
+  a.n_rows = keys.n_rows;
+  a.q_pos0 = q_pos0;
+  a.NQ = (Q >= 4 && p.H_I <= 64) ? 256 / p.H_I : (Q >= 2 && p.H_I <= 128 ? 256 / p.H_I : 1);
+  if (a.NQ > 4) a.NQ = 4;
+  if (a.NQ > Q) a.NQ = 1;
+  a.nQB = (Q + a.NQ - 1) / a.NQ;
+  a.tps = (int)ceil_div(N, kTileKeys);
+  const int NM = a.NQ * p.H_I;
+  const int epi_wg = (NM == 256 && a.NQ >= 2) ? 2 : 1;
+  const int esz = fp8 ? 1 : 2;
+  a.chunk_elems = 128 / esz;
+  a.n_chunks = p.d_I * esz / 128;
+  a.ksteps = p.d_I * esz / 32;
+  a.a_chunk_bytes = kTileKeys * 128;
+  a.b_chunk_bytes = NM * 128;
+  a.a_bytes = a.a_chunk_bytes * a.n_chunks;
+  a.b_bytes = a.b_chunk_bytes * a.n_chunks;
+  const size_t budget = 220 * 1024;
+  // two query buffers when that still leaves a ring of at least 4 key stages
+  a.nb = (2 * (size_t)a.b_bytes + 4 * (size_t)a.a_bytes <= budget - 1024) ? 2 : 1;
+  int stages = (int)((budget - 1024 - a.nb * (size_t)a.b_bytes) / a.a_bytes);
+  if (stages > 8) stages = 8;
+  if (stages < 2) return cudaErrorNotSupported;
+  a.stages = stages;
+  a.tmem_cols = (uint32_t)pow2_at_least(2 * NM);
+  if (a.tmem_cols > 512) return cudaErrorNotSupported;
+  const bool all_visible = n_vis(q_pos0, p.m) >= N;
+  a.mode = all_visible ? 0 : 1;
+  a.total = all_visible ? (int64_t)p.B * a.nQB * a.tps : (int64_t)p.B * a.nQB;
+  a.w = w;
+  a.q_scale = q_scale;
+  a.k_scale = keys.scale;
+  a.scores = scores;
+
+  CUtensorMap tm_keys, tm_q;
+  if (!make_map(&tm_keys, keys.data, fp8, (int64_t)p.B * keys.n_rows, p.d_I, kTileKeys))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tm_q, q_idx, fp8, (int64_t)p.B * Q * p.H_I, p.d_I, NM)) return cudaErrorInvalidValue;
+
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t grid = sms;
+  if (a.total < grid) grid = a.total;
+  if (grid < 1) grid = 1;
+  const size_t smem = 1024 + (size_t)a.stages * a.a_bytes + (size_t)a.nb * a.b_bytes +
+                      (2 * a.stages + 9) * sizeof(uint64_t) + 16;
+  const int threads = 64 + 128 * epi_wg;
+  cudaError_t e;
+#define CSA_LAUNCH_TC(FP8, EW)                                                                  \
+  do {                                                                                          \
+    e = cudaFuncSetAttribute(index_tc_kernel<FP8, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             (int)smem);                                                        \
+    if (e != cudaSuccess) return e;                                                             \
+    index_tc_kernel<FP8, EW><<<(unsigned)grid, threads, smem, st>>>(tm_keys, tm_q, a);          \
+  } while (0)
+  if (fp8) {
+    if (epi_wg == 2) CSA_LAUNCH_TC(true, 2); else CSA_LAUNCH_TC(true, 1);
+  } else {
+    if (epi_wg == 2) CSA_LAUNCH_TC(false, 2); else CSA_LAUNCH_TC(false, 1);
+  }
+#undef CSA_LAUNCH_TC
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (fill_invisible && !all_visible) {
+    fill_invisible_kernel<<<(unsigned)((int64_t)p.B * Q), 256, 0, st>>>(scores, Q, N, p.m, q_pos0);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace csa

@@ -74,6 +74,15 @@ class Step:
         n = wl.B * wl.Q * wl.k
         return self.ws[off: off + n * 4].view(torch.int32).view(wl.B, wl.Q, wl.k)
 
+    def launches_per_step(self) -> int:
+        """Kernels one run() launches (as the library's launch plan stands)."""
+        wl = self.wl
+        attend = 1 + (1 if csa.workspace_size(self.p, csa.WS_HCA if wl.mode.startswith("hca")
+                                              else csa.WS_ATTEND, wl.Q, wl.N) else 0)
+        if wl.mode.startswith("hca"):
+            return 1 + attend
+        return 2 + 1 + csa.topk_launches(self.p, wl.Q, wl.N) + attend
+
     def run(self, stream=None):
         wl = self.wl
         if wl.mode.startswith("csa"):

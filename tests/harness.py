@@ -105,14 +105,17 @@ class SeqOracle:
                             wl.W, wl.D_v, wl.scale)
 
 
-def check_scores(gpu: np.ndarray, ref: np.ndarray):
-    """GPU fp32 scores against float64: -inf pattern exact, finite values
-    within 1e-5 of the row's scale (fp32 accumulation of a few thousand
-    products)."""
-    assert np.array_equal(np.isinf(gpu), np.isinf(ref)), "visibility pattern differs"
+def check_scores(gpu: np.ndarray, ref: np.ndarray, check_invisible: bool = False):
+    """GPU fp32 scores against float64 on every visible entry (finite in the
+    oracle): within 1e-5 of the row's scale (fp32 accumulation of a few
+    thousand products).  The invisible part is compared (-inf) only when
+    asked: the fused forward leaves it unwritten, since top-k never reads it."""
     fin = np.isfinite(ref)
+    if check_invisible:
+        assert np.array_equal(np.isinf(gpu), ~fin), "visibility pattern differs"
     if not fin.any():
         return 0.0
+    assert np.all(np.isfinite(gpu[fin])), "a visible score is not finite"
     row_scale = np.where(fin, np.abs(ref), 0).max(axis=1, keepdims=True) + 1e-30
     err = np.abs(np.where(fin, gpu, 0) - np.where(fin, ref, 0)) / row_scale
     worst = float(err[fin].max())

@@ -1,0 +1,74 @@
+"""Parity at the full size of the timed workload: CSA decode at 1M-token
+context, B = 32 (262,144 entries per sequence), in the launch configuration
+bench.py times (one csa_forward per step).  Every sequence: the compressed
+tail entry and key bit-exact, every visible score within 1e-5 of the row
+scale, the selection within the swap rule; the attention output on a fixed
+sample of 8 sequences (the oracle evaluates the 1152 keys each query keeps)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from long_context_sparse_25_b300 import synth
+from long_context_sparse_25_b300.pipeline import Step
+
+from harness import check_out, check_scores, check_selection, f64
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _decode_parity(wl, dev, attn_seqs):
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    N, m = wl.N, wl.m
+    pos = np.array([wl.q_pos0])
+    sel_all = step.selected().cpu().numpy()
+    out = f64(step.out)
+    mixed = wl.dtype == "mixed"
+    for b in range(wl.B):
+        x, g = f64(inp["x"][b]), f64(inp["g"][b])
+        xi, gi = f64(inp["xi"][b]), f64(inp["gi"][b])
+        a = (N - 1) * m - wl.raw_pos0
+        new_key = O.store_rows(O.compress(xi[a:a + m], gi[a:a + m], f64(inp["bias_i"]), m),
+                               "e4m3" if mixed else "bf16")
+        new_kv = O.store_rows(O.compress(x[a:a + m], g[a:a + m], f64(inp["bias"]), m),
+                              "e4m3" if mixed else "bf16", wl.D_v)
+        if mixed:
+            keys = O.dequantize_rows_e4m3(inp["keys"][b].cpu().view(torch.uint8).numpy(),
+                                          inp["keys_scale"][b].cpu().numpy())
+            qi = O.dequantize_rows_e4m3(inp["q_idx"][b].cpu().view(torch.uint8).numpy(),
+                                        inp["q_idx_scale"][b].cpu().numpy())
+        else:
+            keys = f64(inp["keys"][b])
+            qi = f64(inp["q_idx"][b])
+        # the GPU's tail rows were written in place; they must equal the oracle's
+        assert np.array_equal(keys[N - 1], new_key[0]), f"seq {b}: tail indexer key"
+        keys = np.array(keys)
+        keys[N - 1] = new_key[0]
+        ref = O.index_scores(qi, f64(inp["w"][b]), keys, pos, m)
+        check_scores(step.scores()[b].cpu().double().numpy(), ref)
+        check_selection(sel_all[b], ref, O.n_vis(pos, m), wl.k)
+        if b in attn_seqs:
+            s = sel_all[b, 0]
+            s = s[s >= 0]
+            rows = torch.from_numpy(s).to(dev).long()
+            if mixed:
+                ent = O.dequantize_rows_e4m3(inp["kv_nope"][b][rows].cpu().view(torch.uint8).numpy(),
+                                             inp["kv_scale"][b][rows].cpu().numpy(),
+                                             inp["kv_rope"][b][rows].cpu().view(torch.int16).numpy().view(np.uint16))
+            else:
+                ent = f64(inp["kv"][b][rows])
+            last = np.flatnonzero(s == N - 1)
+            if last.size:
+                assert np.array_equal(ent[last[0]], new_kv[0]), f"seq {b}: tail entry"
+            o = O.csa_attend(f64(inp["q"][b]), ent, x, wl.raw_pos0, np.arange(s.size)[None], pos,
+                             wl.W, wl.D_v, wl.scale)
+            check_out(out[b], o, False)
+
+
+def test_decode_1m_full_size(cuda_device):
+    wl = synth.WORKLOADS["csa_decode_1m"]
+    _decode_parity(wl, cuda_device, attn_seqs={0, 5, 11, 16, 21, 26, 30, 31})
