@@ -135,9 +135,12 @@ extern "C" {
 const char* csa_last_error(void) { return g_err; }
 
 int csa_device_status(csa_stream_t stream) {
-  int code = 0;
+  int code = 0, code2 = 0;
   cudaError_t e = index_tc_status(&code, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "csa_device_status");
+  e = attend_tc_status(&code2, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "csa_device_status");
+  if (code == 0) code = code2;
   if (code != 0)
     return fail(CSA_ERR_TIMEOUT, "a bounded device-side wait gave up (site %d); the outputs of the "
                                  "calls since the last check are not valid", code);

@@ -9,7 +9,9 @@
 // the latent, the decoupled RoPE key only enters the score);
 // "DeepSeek-V4 详解" section 2.2 Step 4 and 2.3 Step 2.
 //
-// This is the CUDA-core path (fp32 arithmetic), used for every dtype.  A CTA
+// This is the CUDA-core path (fp32 arithmetic): the fp32 workloads, whose
+// 1e-4 bound rules out bf16 operands, and shapes the tensor-core path
+// (attend_tc.cu) does not take.  A CTA
 // takes 16 heads of one query and one split of its key list; keys are staged
 // in shared memory in tiles of 32 rows converted to fp32.  Splits of the key
 // list are fixed by the key-list length alone (never by the batch), and their
@@ -18,6 +20,15 @@
 #include "common.cuh"
 
 namespace csa {
+
+bool attend_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& kv,
+                         const csa_rows& raw, int Q, int64_t N, csa_dtype out_dtype);
+size_t attend_tc_workspace(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0);
+cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows& kv,
+                             const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                             int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
+                             void* ws, cudaStream_t st);
+
 namespace {
 
 constexpr int kHG = 16;       // heads per CTA
@@ -238,12 +249,18 @@ void split_plan(const csa_params& p, int Q, int64_t N, bool dense, int* splits, 
 
 }  // namespace
 
+// Scratch of either path (the dtypes that pick the path are not known here):
+// the larger of the CUDA-core split partials and the tensor-core ones.  The
+// tensor-core plan is largest for the latest query, which sees the most
+// entries, so that position bounds it for every q_pos0.
 size_t attend_workspace(const csa_params& p, int Q, int64_t N, bool dense) {
   int splits;
   int64_t split_len;
   split_plan(p, Q, N, dense, &splits, &split_len);
-  if (splits <= 1) return 0;
-  return (size_t)p.B * Q * p.H * splits * (p.D_v + 2) * sizeof(float);
+  size_t simt = 0;
+  if (splits > 1) simt = (size_t)p.B * Q * p.H * splits * (p.D_v + 2) * sizeof(float);
+  const size_t tc = attend_tc_workspace(p, Q, N, dense, (int64_t)1 << 62);
+  return simt > tc ? simt : tc;
 }
 
 cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype, const csa_rows& kv,
@@ -252,6 +269,9 @@ cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype,
                           void* ws, cudaStream_t st) {
   const int64_t rows = (int64_t)p.B * Q;
   if (rows <= 0) return cudaSuccess;
+  if (attend_tc_supported(p, q_dtype, kv, raw, Q, N, out_dtype))
+    return launch_attend_tc(p, q, kv, raw, raw_pos0, idx, dense, q_pos0, Q, N, out, out_dtype, ws,
+                            st);
   int splits;
   int64_t split_len;
   split_plan(p, Q, N, dense, &splits, &split_len);

@@ -1,0 +1,831 @@
+// Tensor-core path of steps 4 / 5 (CSA sparse MQA, HCA dense MQA): tcgen05
+// MMAs with TMEM accumulators, keys gathered by TMA into a ring of
+// 128-byte-swizzled shared-memory chunks.
+//
+//   o[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . K_j) * K_j[0:D_v]
+//
+// Sources: "一文搞懂 DeepSeek：从 V3 的 KV 压缩与 MoE，到 V4 的百万 token 上下文",
+// section "V4 改进一：CSA 与 HCA" (selected entries plus a sliding window of
+// raw KV, one KV shared by all heads: MQA; HCA attends densely) and section
+// "V3 看家本领一：MLA" (the value is the latent, the decoupled RoPE key only
+// enters the score); "DeepSeek-V4 详解" section 2.2 Step 4 (bf16, 128 heads)
+// and section 2.3 Step 2.
+//
+// Mapping.  The 128 heads of one query are the MMA's M side, so one shared
+// key row feeds every head.  A 128 x 512 fp32 output accumulator alone fills
+// all 512 TMEM columns, so each CTA owns one half of the value dims (256
+// columns) and computes the 128 x 128 score tile S = Q K^T itself (both halves
+// of a query compute the same S; the extra QK^T work buys an accumulator that
+// fits).  TMEM: two S buffers (columns 0-255) and O (columns 256-511).  After
+// the softmax reads S it writes P (bf16 pairs) over the first 64 columns of
+// the same buffer, and P . V runs with A taken from TMEM.
+//
+// Shared memory: Q of the query (D_qk/64 chunks of 128 x 64 bf16, resident)
+// and a ring of kRing chunks of 128 keys x 64 dims.  For every tile of 128
+// keys the producer gathers the D_qk/64 chunks of the keys (TMA gather4 of
+// four rows at a time) and then, one tile later, the D_v/128 chunks of the
+// value half.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims
+// in bf16) are converted by the producer warp itself: for QK^T each
+// dequantised key is split exactly into a bf16 high part and a bf16 low part
+// (two chunk loads per nope chunk, both multiplied by the same Q chunk), so
+// the scores see the key to about 2^-17; for PV the chunk holds the codes
+// themselves (exact in bf16) and the row scale is folded into P, which is
+// split the same way (PV runs on the high and on the low part).  The
+// MMA order is S(0), S(1), PV(0), S(2), PV(1), ... so the softmax of tile u
+// overlaps S(u+1).  A key row doubles as its value row: the same 128-byte
+// swizzled chunk is K-major for QK^T and MN-major for PV.
+//
+// Softmax: one thread per head row, log2 domain, running maximum updated only
+// when a tile's maximum exceeds it by more than 2^8 (then O and the running
+// sum are rescaled); P = 2^(x - m) <= 2^8 fits bf16 and fp32 comfortably.
+//
+// Decode (one query per sequence) splits the key list into fixed runs of
+// tiles (chosen from the key-list length only, never from the batch) and
+// merges the splits in order in attend_tc_combine_kernel.
+//
+// Roles: warp 0 producer, warp 1 TMEM allocator + MMA issuer (one thread),
+// warps 2-5 softmax / rescale / epilogue.  Every mbarrier wait is bounded; a
+// timeout is recorded in a device error word and the kernel returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace csa {
+
+namespace {
+
+__device__ int g_attend_tc_error = 0;
+
+constexpr int kT = 128;              // keys per tile
+constexpr int kRing = 5;             // key chunk slots
+constexpr uint32_t kChunk = 16384;   // 128 rows x 128 bytes
+constexpr int kMaxQChunks = 9;       // D_qk <= 576
+constexpr float kRescaleLog2 = 8.f;  // rescale when the maximum grows by more than 2^8
+constexpr int kThreads = 192;
+
+struct AttArgs {
+  int B, Q, H, D_qk, D_v, k, W, m;
+  int nc;   // D_qk / 64
+  int nsc;  // key chunk loads per tile for QK^T (nc, plus nope/64 low parts for e4m3)
+  int nvc;  // D_v / 128: value chunks per half
+  int dense;
+  int e4m3;
+  int splits, tps;  // splits per (query, half); tiles per split
+  int64_t N, kv_rows, raw_rows, raw_pos0, q_pos0;
+  float c_log2;  // scale * log2(e)
+  const int32_t* idx;
+  const uint8_t* codes;  // e4m3 entries: [B, kv_rows, nope]
+  const uint16_t* rope;  // [B, kv_rows, D_qk - nope]
+  const float* kscale;   // [B, kv_rows]
+  int nope;
+  const uint16_t* raw16;  // raw rows (e4m3 path reads the window itself)
+  void* out;
+  int out_f32;
+  float* part;  // splits > 1: [rows*H][splits][D_v] unnormalised O
+  float* ml;    // splits > 1: [rows*H][splits][2] (max, sum), log2 domain
+};
+
+struct KeyList {
+  int64_t t, lo;
+  int kd;     // entry slots with meaning (k, or the visible entries for HCA)
+  int k_ent;  // entry part rounded up to a multiple of 4 (gather groups never straddle)
+  int w_len;  // window tokens
+  int len;    // k_ent + w_len
+};
+
+__device__ __forceinline__ KeyList key_list(const AttArgs& a, int i) {
+  KeyList kl;
+  kl.t = a.q_pos0 + i;
+  kl.lo = kl.t - a.W + 1 > 0 ? kl.t - a.W + 1 : 0;
+  kl.w_len = a.W > 0 ? (int)(kl.t - kl.lo + 1) : 0;
+  if (a.dense) {
+    int64_t nv = n_vis(kl.t, a.m);
+    kl.kd = (int)(nv < a.N ? nv : a.N);
+  } else {
+    kl.kd = a.k;
+  }
+  kl.k_ent = (kl.kd + 3) & ~3;
+  kl.len = kl.k_ent + kl.w_len;
+  return kl;
+}
+
+// Rows of the four key slots j0..j0+3 (j0 % 4 == 0): entry rows index the
+// entry cache, window rows the raw rows; invalid slots point at a valid row
+// and are masked in the softmax.
+struct Group {
+  int rows[4];
+  int win;       // 1: rows of the raw-row tensor
+  uint32_t vmask;  // bit q: slot j0+q holds a key
+};
+
+__device__ __forceinline__ Group group_rows(const AttArgs& a, const KeyList& kl, int b,
+                                            int64_t qrow, int j0) {
+  Group g;
+  g.vmask = 0;
+  if (j0 < kl.k_ent || a.W == 0) {
+    g.win = 0;
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      int64_t e = 0;
+      bool v = false;
+      if (j < kl.kd) {
+        if (a.dense) {
+          e = j;
+          v = true;
+        } else {
+          e = a.idx[qrow * (int64_t)a.k + j];
+          v = e >= 0 && e < a.N;  // -1 (and anything out of range) is an empty slot
+          if (!v) e = 0;
+        }
+      }
+      g.rows[q] = (int)((int64_t)b * a.kv_rows + e);
+      g.vmask |= (v ? 1u : 0u) << q;
+    }
+  } else {
+    g.win = 1;
+    const int w0 = j0 - kl.k_ent;
+    for (int q = 0; q < 4; ++q) {
+      const bool v = w0 + q < kl.w_len;
+      const int64_t pos = kl.lo + (v ? w0 + q : 0);
+      g.rows[q] = (int)((int64_t)b * a.raw_rows + (pos - a.raw_pos0));
+      g.vmask |= (v ? 1u : 0u) << q;
+    }
+  }
+  return g;
+}
+
+// 16 bytes of a 128-byte swizzled row: unit u of row r of a chunk.
+__device__ __forceinline__ uint32_t swz(int r, int u) {
+  return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+// Mixed-precision cache: one chunk of 128 key rows x 64 dims written by the
+// producer warp itself (lane l: slots 4l..4l+3), as bf16.
+//   kHi:  dequantised nope dims, rounded to bf16 (RoPE dims and window rows:
+//         their bf16 values);
+//   kLo:  the rounding error of kHi, rounded to bf16 (window rows: 0);
+//   kVal: the e4m3 codes as bf16 (exact; the row scale goes into P), window
+//         rows as they are.
+enum ChunkMode { kHi = 0, kLo = 1, kVal = 2 };
+
+__device__ void manual_chunk(const AttArgs& a, uint8_t* dst, const Group& g, int c, int mode) {
+  const int lane = threadIdx.x & 31;
+  for (int q = 0; q < 4; ++q) {
+    const int r = lane * 4 + q;
+    const int64_t row = g.rows[q];
+    uint4 v[8];
+    if (g.win) {
+      if (mode == kLo) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + c * 64);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u);
+      }
+    } else if (c * 64 < a.nope) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.codes + row * a.nope + c * 64);
+      const float sc = mode == kVal ? 1.f : __ldg(a.kscale + row);
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const uint4 cv = __ldg(src + u4);
+        const uint32_t w4[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t word = w4[h * 2 + e / 2];
+            const int sh = (e & 1) * 16;
+            // code * scale in fp32 is within 2^-24 of the exact product; the
+            // high part is its bf16 rounding, the low part the (exact) rest
+            float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * sc;
+            float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * sc;
+            if (mode == kLo) {
+              f0 -= __bfloat162float(__float2bfloat16_rn(f0));
+              f1 -= __bfloat162float(__float2bfloat16_rn(f1));
+            }
+            o[e] = pack_bf16(f0, f1);
+          }
+          v[u4 * 2 + h] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else {
+      if (mode == kLo) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const int rw = a.D_qk - a.nope;
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.rope + row * rw + (c * 64 - a.nope));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(dst + swz(r, u)) = v[u];
+  }
+  tc::fence_proxy_async_smem();
+}
+
+template <bool kE4M3>
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_raw, const AttArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sRing = sQ + (size_t)a.nc * kChunk;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + (size_t)kRing * kChunk);
+  uint64_t* ring_full = bars;
+  uint64_t* ring_empty = bars + kRing;
+  uint64_t* q_full = bars + 2 * kRing;
+  uint64_t* s_full = q_full + 1;      // [2]
+  uint64_t* p_full = s_full + 2;      // [2]
+  uint64_t* mask_full = p_full + 2;   // [2]
+  uint64_t* mask_empty = mask_full + 2;  // [2]
+  uint64_t* o_done = mask_empty + 2;
+  uint64_t* mma_done = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint32_t* smask = tmem_slot + 4;  // [2][4] ballot words of the tile's valid slots
+  float* svscale = reinterpret_cast<float*>(smask + 8);  // e4m3: [2][128] row scales of the tile
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* err = &g_attend_tc_error;
+
+  // work item: (query row, value half, split)
+  const int split = (int)(blockIdx.x % a.splits);
+  const int half = (int)((blockIdx.x / a.splits) & 1);
+  const int64_t qrow = blockIdx.x / ((int64_t)a.splits * 2);  // b * Q + i
+  const int i = (int)(qrow % a.Q);
+  const int b = (int)(qrow / a.Q);
+  const KeyList kl = key_list(a, i);
+  const int n_tiles_all = (kl.len + kT - 1) / kT;
+  const int tile0 = split * a.tps;
+  int n = n_tiles_all - tile0;
+  if (n > a.tps) n = a.tps;
+  if (n < 0) n = 0;
+  const int vc0 = half * a.nvc;  // first key chunk that is a value chunk of this half
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      tc::mbar_init(&ring_full[s], 1);
+      tc::mbar_init(&ring_empty[s], 1);
+    }
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&p_full[s], 4);
+      tc::mbar_init(&mask_full[s], 1);
+      tc::mbar_init(&mask_empty[s], 4);
+    }
+    tc::mbar_init(o_done, 1);
+    tc::mbar_init(mma_done, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tm_q);
+    if (!kE4M3) tc::prefetch_tmap(&tm_kv);
+    if (a.W > 0 && !kE4M3) tc::prefetch_tmap(&tm_raw);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && n > 0) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    if (lane == 0) {
+      tc::mbar_expect_tx(q_full, a.nc * kChunk);
+      for (int c = 0; c < a.nc; ++c)
+        tc::tma_load_2d(sQ + c * kChunk, &tm_q, q_full, c * 64, (int)(qrow * a.H));
+    }
+    uint32_t lt = 0;
+    auto load_chunk = [&](int c, int mode, const Group& g) -> bool {
+      const uint32_t slot = lt % kRing;
+      int okw = 1;
+      if (lane == 0) okw = tc::mbar_wait(&ring_empty[slot], ((lt / kRing) & 1) ^ 1, err, 11);
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) return false;
+      uint8_t* dst = sRing + slot * kChunk;
+      if (kE4M3) {
+        manual_chunk(a, dst, g, c, mode);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&ring_full[slot]);
+      } else {
+        if (lane == 0) tc::mbar_expect_tx(&ring_full[slot], kChunk);
+        __syncwarp();
+        tc::tma_gather4(dst + lane * 512, g.win ? &tm_raw : &tm_kv, &ring_full[slot], c * 64,
+                        g.rows[0], g.rows[1], g.rows[2], g.rows[3]);
+      }
+      ++lt;
+      return true;
+    };
+    Group prev{};
+    for (int u = 0; u <= n && ok; ++u) {
+      Group cur{};
+      if (u < n) {
+        cur = group_rows(a, kl, b, qrow, (tile0 + u) * kT + lane * 4);
+        // validity ballots of the tile for the softmax
+        int okw = 1;
+        if (lane == 0) okw = tc::mbar_wait(&mask_empty[u & 1], ((u >> 1) & 1) ^ 1, err, 12);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) break;
+        uint32_t bal[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bal[q] = __ballot_sync(0xffffffffu, (cur.vmask >> q) & 1);
+        if (lane < 4) smask[(u & 1) * 4 + lane] = bal[lane];
+        if (kE4M3) {
+          // scale of each slot's value row (1 for window rows and empty slots)
+          for (int q = 0; q < 4; ++q) {
+            float sc = 1.f;
+            if (!cur.win && ((cur.vmask >> q) & 1)) sc = __ldg(a.kscale + cur.rows[q]);
+            svscale[(u & 1) * 128 + lane * 4 + q] = sc;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
+        for (int cc = 0; cc < a.nsc && ok; ++cc)
+          ok = cc < a.nc ? load_chunk(cc, kHi, cur) : load_chunk(cc - a.nc, kLo, cur);
+      }
+      if (u >= 1)
+        for (int c = 0; c < a.nvc && ok; ++c) ok = load_chunk(vc0 + c, kVal, prev);
+      prev = cur;
+    }
+    // let this CTA's copies in flight land before it can exit
+    if (!kE4M3 && lane == 0)
+      for (uint32_t j = lt > (uint32_t)kRing ? lt - kRing : 0; j < lt; ++j)
+        tc::mbar_drain(&ring_full[j % kRing], (j / kRing) & 1);
+    if (lane == 0) tc::mbar_drain(q_full, 0);
+  } else if (warp == 1 && n > 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = tc::idesc(128, kT, 1, 1);
+      const uint32_t id_pv = tc::idesc(128, 64, 1, 1, 0, 1);
+      uint32_t lt = 0;
+      bool ok = tc::mbar_wait(q_full, 0, err, 21);
+      const uint32_t q0 = tc::smem_u32(sQ);
+      const uint32_t r0 = tc::smem_u32(sRing);
+      auto issue_pv = [&](int u) -> bool {
+        const uint32_t sb = u & 1;
+        if (!tc::mbar_wait(&p_full[sb], (u >> 1) & 1, err, 22)) return false;
+        tc::tc_fence_after();
+        for (int c = 0; c < a.nvc; ++c) {
+          const uint32_t slot = lt % kRing;
+          if (!tc::mbar_wait(&ring_full[slot], (lt / kRing) & 1, err, 23)) return false;
+          tc::tc_fence_after();
+          for (int ks = 0; ks < kT / 16; ++ks) {
+            const uint64_t bd = tc::sdesc_sw128_mn(r0 + slot * kChunk + ks * 2048);
+            tc::mma_bf16_ts(tmem + 256 + 64 * c, tmem + sb * 128 + 8 * ks, bd, id_pv,
+                            (u > 0 || ks > 0) ? 1u : 0u);
+            if (kE4M3)  // the low part of P
+              tc::mma_bf16_ts(tmem + 256 + 64 * c, tmem + sb * 128 + 64 + 8 * ks, bd, id_pv, 1u);
+          }
+          tc::mma_commit(&ring_empty[slot]);
+          ++lt;
+        }
+        tc::mma_commit(o_done);
+        return true;
+      };
+      for (int u = 0; u < n && ok; ++u) {
+        const uint32_t sb = u & 1;
+        for (int cc = 0; cc < a.nsc && ok; ++cc) {
+          const int c = cc < a.nc ? cc : cc - a.nc;  // the Q chunk this key chunk meets
+          const uint32_t slot = lt % kRing;
+          if (!tc::mbar_wait(&ring_full[slot], (lt / kRing) & 1, err, 24)) { ok = false; break; }
+          tc::tc_fence_after();
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = tc::sdesc_sw128(q0 + c * kChunk + ks * 32);
+            const uint64_t bd = tc::sdesc_sw128(r0 + slot * kChunk + ks * 32);
+            tc::mma_bf16(tmem + sb * 128, ad, bd, id_s, (cc > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&ring_empty[slot]);
+          ++lt;
+        }
+        if (!ok) break;
+        tc::mma_commit(&s_full[sb]);
+        if (u >= 1) ok = issue_pv(u - 1);
+      }
+      if (ok) issue_pv(n - 1);
+      // every MMA issued must have completed before TMEM is released
+      tc::mma_commit(mma_done);
+      tc::mbar_drain(mma_done, 0);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int u = 0; u < n && ok; ++u) {
+      const uint32_t sb = u & 1;
+      // every lane acquires the producer's ballot words itself
+      const bool mk = tc::mbar_wait(&mask_full[sb], (u >> 1) & 1, err, 31);
+      if (!__all_sync(0xffffffffu, mk)) { ok = false; break; }
+      uint32_t bal[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        bal[q] = *reinterpret_cast<volatile uint32_t*>(&smask[sb * 4 + q]);
+      __syncwarp();
+      if (!kE4M3 && lane == 0) tc::mbar_arrive(&mask_empty[sb]);
+      int okw = lane == 0 ? (int)tc::mbar_wait(&s_full[sb], (u >> 1) & 1, err, 32) : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      if (!okw) { ok = false; break; }
+      tc::tc_fence_after();
+      float x[kT];
+#pragma unroll
+      for (int g = 0; g < kT / 32; ++g) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_base + sb * 128 + g * 32, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) x[g * 32 + jj] = __uint_as_float(r[jj]);
+      }
+      float m_tile = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kT; ++j) {
+        const bool v = (bal[j & 3] >> (j >> 2)) & 1u;
+        x[j] = v ? x[j] * a.c_log2 : -INFINITY;
+        m_tile = fmaxf(m_tile, x[j]);
+      }
+      const bool grow = m_tile > m_ref + kRescaleLog2;
+      const bool rescale = grow && m_ref != -INFINITY;
+      const float alpha = grow ? exp2f(m_ref - m_tile) : 1.f;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O holds the tiles before u: wait for PV(u-1), then scale the rows
+        okw = lane == 0 ? (int)tc::mbar_wait(o_done, (u - 1) & 1, err, 33) : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        __syncwarp();
+        if (!okw) { ok = false; break; }
+        tc::tc_fence_after();
+        const float f = rescale ? alpha : 1.f;
+        for (int g = 0; g < 256 / 32; ++g) {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem + lane_base + 256 + g * 32, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(__uint_as_float(r[jj]) * f);
+          tc::tmem_st32(tmem + lane_base + 256 + g * 32, r);
+        }
+        tc::tmem_wait_st();
+      }
+      if (grow) {
+        l_run *= alpha;
+        m_ref = m_tile;
+      }
+      // P = 2^(x - m_ref) as bf16 pairs over the first 64 columns of the buffer
+      // (mixed caches: P times the value row's scale, split exactly into a
+      // bf16 high part in columns 0-63 and a bf16 low part in columns 64-127)
+#pragma unroll
+      for (int j = 0; j < kT; ++j) {
+        const float pj = m_ref == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
+        l_run += pj;
+        x[j] = kE4M3 ? pj * svscale[sb * 128 + j] : pj;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(x[hh * 64 + 2 * c], x[hh * 64 + 2 * c + 1]);
+        tc::tmem_st32(tmem + lane_base + sb * 128 + hh * 32, pk);
+      }
+      if (kE4M3) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float a0 = x[hh * 64 + 2 * c], a1 = x[hh * 64 + 2 * c + 1];
+            pk[c] = pack_bf16(a0 - __bfloat162float(__float2bfloat16_rn(a0)),
+                              a1 - __bfloat162float(__float2bfloat16_rn(a1)));
+          }
+          tc::tmem_st32(tmem + lane_base + sb * 128 + 64 + hh * 32, pk);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (kE4M3) tc::mbar_arrive(&mask_empty[sb]);
+        tc::mbar_arrive(&p_full[sb]);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    bool have_o = ok && n > 0;
+    if (have_o) {
+      // PV(n-3) has completed (it precedes S(n-1)), so o_done has finished at
+      // least n-2 phases: wait for phase n-2, then n-1, one parity at a time
+      int okw = 1;
+      if (lane == 0) {
+        if (n >= 2) okw = tc::mbar_wait(o_done, (n - 2) & 1, err, 34);
+        if (okw) okw = tc::mbar_wait(o_done, (n - 1) & 1, err, 35);
+      }
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      have_o = okw != 0;
+      tc::tc_fence_after();
+    }
+    if (ok) {
+      const int hv = a.D_v / 2;
+      const int64_t orow = qrow * a.H + h;
+      if (a.splits == 1) {
+        const float inv = (have_o && l_run > 0.f) ? 1.f / l_run : 0.f;
+        for (int g = 0; g < hv / 32; ++g) {
+          uint32_t r[32];
+          if (have_o) {
+            tc::tmem_ld32(tmem + lane_base + 256 + g * 32, r);
+            tc::tmem_wait_ld();
+          }
+          const int64_t o0 = orow * a.D_v + half * hv + g * 32;
+          if (a.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + o0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 o;
+              o.x = have_o ? __uint_as_float(r[4 * v + 0]) * inv : 0.f;
+              o.y = have_o ? __uint_as_float(r[4 * v + 1]) * inv : 0.f;
+              o.z = have_o ? __uint_as_float(r[4 * v + 2]) * inv : 0.f;
+              o.w = have_o ? __uint_as_float(r[4 * v + 3]) * inv : 0.f;
+              dst[v] = o;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + o0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float f0 = have_o ? __uint_as_float(r[8 * v + 2 * e]) * inv : 0.f;
+                const float f1 = have_o ? __uint_as_float(r[8 * v + 2 * e + 1]) * inv : 0.f;
+                w[e] = pack_bf16(f0, f1);
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      } else {
+        const int64_t prow = orow * a.splits + split;
+        float4* dst = reinterpret_cast<float4*>(a.part + prow * a.D_v + half * hv);
+        for (int g = 0; g < hv / 32; ++g) {
+          uint32_t r[32];
+          if (have_o) {
+            tc::tmem_ld32(tmem + lane_base + 256 + g * 32, r);
+            tc::tmem_wait_ld();
+          }
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 o;
+            o.x = have_o ? __uint_as_float(r[4 * v + 0]) : 0.f;
+            o.y = have_o ? __uint_as_float(r[4 * v + 1]) : 0.f;
+            o.z = have_o ? __uint_as_float(r[4 * v + 2]) : 0.f;
+            o.w = have_o ? __uint_as_float(r[4 * v + 3]) : 0.f;
+            dst[g * 8 + v] = o;
+          }
+        }
+        if (half == 0) {
+          a.ml[prow * 2 + 0] = have_o ? m_ref : -INFINITY;
+          a.ml[prow * 2 + 1] = have_o ? l_run : 0.f;
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the splits of one (query, head) in split order (log2 domain).
+__global__ void __launch_bounds__(128) attend_tc_combine_kernel(const float* __restrict__ part,
+                                                                const float* __restrict__ ml,
+                                                                int splits, int D_v,
+                                                                void* __restrict__ out,
+                                                                int out_f32) {
+  const int64_t qh = blockIdx.x;
+  const float* mlr = ml + qh * splits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, mlr[2 * s]);
+  float L = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float ms = mlr[2 * s];
+    if (ms != -INFINITY) L += mlr[2 * s + 1] * exp2f(ms - M);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  for (int d4 = threadIdx.x; d4 < D_v / 4; d4 += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < splits; ++s) {
+      const float ms = mlr[2 * s];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      const float4 p = reinterpret_cast<const float4*>(part + (qh * splits + s) * D_v)[d4];
+      acc.x = fmaf(p.x, f, acc.x);
+      acc.y = fmaf(p.y, f, acc.y);
+      acc.z = fmaf(p.z, f, acc.z);
+      acc.w = fmaf(p.w, f, acc.w);
+    }
+    if (out_f32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + qh * D_v)[d4] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      uint2 w;
+      w.x = pack_bf16(acc.x * inv, acc.y * inv);
+      w.y = pack_bf16(acc.z * inv, acc.w * inv);
+      reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + qh * D_v)[d4] = w;
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] bf16 matrix: box of 64 columns
+// (128 bytes) x box_rows, 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Longest key list of the launch, in tiles.
+int max_tiles(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0) {
+  int64_t kd;
+  if (dense) {
+    kd = n_vis(q_pos0 + Q - 1, p.m);
+    if (kd > N) kd = N;
+  } else {
+    kd = p.k;
+  }
+  const int64_t len = ((kd + 3) & ~3ll) + p.window;
+  return (int)ceil_div(len, kT);
+}
+
+}  // namespace
+
+// Split plan of the tensor-core path: one split per (query, half) for
+// multi-query launches; decode (one query per sequence) cuts the key list
+// into at most 16 runs of equal tile counts.  Depends on Q and the key-list
+// length only.
+void attend_tc_plan(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0, int* splits,
+                    int* tps) {
+  const int nt = max_tiles(p, Q, N, dense, q_pos0);
+  if (Q > 1 || nt <= 1) {
+    *splits = 1;
+    *tps = nt > 0 ? nt : 1;
+    return;
+  }
+  const int t = (int)ceil_div(nt, 16);
+  *tps = t;
+  *splits = (int)ceil_div(nt, t);
+}
+
+// Scratch for the split partials.  A shorter key list can take more splits
+// (17 tiles: 9 splits of 2; 16 tiles: 16 splits of 1), so the bound is
+// min(16, tiles of the longest list).
+size_t attend_tc_workspace(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0) {
+  int splits, tps;
+  attend_tc_plan(p, Q, N, dense, q_pos0, &splits, &tps);
+  if (splits <= 1) return 0;
+  const int nt = max_tiles(p, Q, N, dense, q_pos0);
+  splits = nt < 16 ? nt : 16;
+  const size_t rows = (size_t)p.B * Q * p.H * splits;
+  const size_t part = (rows * p.D_v * sizeof(float) + 255) & ~(size_t)255;
+  return part + rows * 2 * sizeof(float);
+}
+
+bool attend_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& kv,
+                         const csa_rows& raw, int Q, int64_t N, csa_dtype out_dtype) {
+  if (q_dtype != CSA_BF16) return false;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return false;
+  if (p.H != 128) return false;
+  if (p.D_qk % 64 != 0 || p.D_qk / 64 > kMaxQChunks) return false;
+  if (p.D_v % 128 != 0 || p.D_v > 512 || p.D_v > p.D_qk) return false;
+  if (N < 1) return false;
+  if (kv.dtype == CSA_E4M3) {
+    if (kv.nope != p.D_v || kv.nope % 64 != 0) return false;
+  } else if (kv.dtype != CSA_BF16) {
+    return false;
+  }
+  if (p.window > 0 && raw.dtype != CSA_BF16) return false;
+  if ((int64_t)p.B * kv.n_rows >= (1ll << 31)) return false;
+  if (p.window > 0 && (int64_t)p.B * raw.n_rows >= (1ll << 31)) return false;
+  if ((int64_t)p.B * Q * p.H >= (1ll << 31)) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t attend_tc_status(int* code, cudaStream_t st) {
+  int h = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_attend_tc_error, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  *code = h;
+  if (h != 0) {
+    int zero = 0;
+    e = cudaMemcpyToSymbol(g_attend_tc_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows& kv,
+                             const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                             int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
+                             void* ws, cudaStream_t st) {
+  AttArgs a{};
+  a.B = p.B;
+  a.Q = Q;
+  a.H = p.H;
+  a.D_qk = p.D_qk;
+  a.D_v = p.D_v;
+  a.k = p.k;
+  a.W = p.window;
+  a.m = p.m;
+  a.nc = p.D_qk / 64;
+  a.nsc = a.nc + (kv.dtype == CSA_E4M3 ? kv.nope / 64 : 0);
+  a.nvc = p.D_v / 128;
+  a.dense = dense ? 1 : 0;
+  a.e4m3 = kv.dtype == CSA_E4M3 ? 1 : 0;
+  a.N = N;
+  a.kv_rows = kv.n_rows;
+  a.raw_rows = p.window > 0 ? raw.n_rows : 0;
+  a.raw_pos0 = raw_pos0;
+  a.q_pos0 = q_pos0;
+  a.c_log2 = p.scale * 1.4426950408889634f;
+  a.idx = idx;
+  a.codes = reinterpret_cast<const uint8_t*>(kv.data);
+  a.rope = reinterpret_cast<const uint16_t*>(kv.rope);
+  a.kscale = kv.scale;
+  a.nope = kv.dtype == CSA_E4M3 ? kv.nope : p.D_qk;
+  a.raw16 = reinterpret_cast<const uint16_t*>(raw.data);
+  a.out = out;
+  a.out_f32 = out_dtype == CSA_F32 ? 1 : 0;
+  attend_tc_plan(p, Q, N, dense, q_pos0, &a.splits, &a.tps);
+  // partials at the front of the workspace, (max, sum) pairs after them
+  const size_t rows = (size_t)p.B * Q * p.H * a.splits;
+  a.part = reinterpret_cast<float*>(ws);
+  a.ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
+                                  ((rows * p.D_v * sizeof(float) + 255) & ~(size_t)255));
+
+  CUtensorMap tm_q, tm_kv, tm_raw;
+  memset(&tm_kv, 0, sizeof(tm_kv));
+  memset(&tm_raw, 0, sizeof(tm_raw));
+  if (!make_map_bf16(&tm_q, q, (int64_t)p.B * Q * p.H, p.D_qk, 128)) return cudaErrorInvalidValue;
+  if (!a.e4m3) {
+    if (!make_map_bf16(&tm_kv, kv.data, (int64_t)p.B * kv.n_rows, p.D_qk, 1))
+      return cudaErrorInvalidValue;
+    if (p.window > 0 && !make_map_bf16(&tm_raw, raw.data, (int64_t)p.B * raw.n_rows, p.D_qk, 1))
+      return cudaErrorInvalidValue;
+  }
+  const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
+                      (2 * kRing + 12) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
+  cudaError_t e;
+  if (a.e4m3) {
+    e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
+  } else {
+    e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  attend_tc_combine_kernel<<<(unsigned)((int64_t)p.B * Q * p.H), 128, 0, st>>>(
+      a.part, a.ml, a.splits, p.D_v, out, a.out_f32);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -89,8 +89,9 @@ cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dty
                          int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
                          bool fill_invisible = true);
 
-// Reads and clears the device error word of the bounded waits (0 = none).
+// Read and clear the device error words of the bounded waits (0 = none).
 cudaError_t index_tc_status(int* code, cudaStream_t st);
+cudaError_t attend_tc_status(int* code, cudaStream_t st);
 
 size_t topk_workspace(const csa_params& p, int Q, int64_t N);
 int topk_launches(const csa_params& p, int Q, int64_t N);

@@ -184,3 +184,60 @@ def test_empty_and_degenerate_cases(cuda_device):
     empty = torch.empty((1, 0, 4, 64), device=cuda_device)
     csa.index(p, empty, torch.empty((1, 0, 4), device=cuda_device), csa.rows(inp["xi"]), 0, 0,
               torch.empty((1, 0, 0), device=cuda_device))
+
+
+@pytest.mark.parametrize("Q,dense", [(1, False), (3, False), (2, True)])
+def test_attend_rescale_holes_and_order(Q, dense, cuda_device):
+    """csa_attend / hca_attend called directly on crafted keys: logits that
+    grow by several nats from one 128-key tile to the next (the running
+    maximum must be raised and the partial output rescaled), -1 holes in the
+    middle of an index list, an index list in descending order, and window
+    rows; compared with the oracle on the same index lists."""
+    rng = np.random.default_rng(11 + Q)
+    B, H, D, Dv, W, m = 2, 128, 576, 512, 5, 4
+    N, k = 700, 400
+    L = N * m + 3
+    q_pos0 = L - Q
+    q = rng.standard_normal((B, Q, H, D)) / np.sqrt(D)
+    kv = rng.standard_normal((B, N, D))
+    # keys aligned with head 0's query, ever more strongly with the entry index
+    # (and so with the tile), so the maximum keeps growing across tiles
+    ramp = np.linspace(0.0, 14.0, N)[None, :, None]
+    kv = kv + ramp * q[:, :1, 0, :] * np.sqrt(D)
+    raw = rng.standard_normal((B, W + Q + 3, D))
+    raw_pos0 = L - raw.shape[1]
+    to_bf = lambda a: torch.from_numpy(O.round_to_bf16(a).astype(np.float32)).to(torch.bfloat16).to(cuda_device)
+    tq, tkv, traw = to_bf(q), to_bf(kv), to_bf(raw)
+    scale = 1.0 / np.sqrt(D)
+    p = csa.params(B, m if not dense else 128, H, D, Dv, 1, 64, k, W, scale)
+    out = torch.empty((B, Q, H, Dv), dtype=torch.bfloat16, device=cuda_device)
+    if dense:
+        n_ent = 300
+        p = csa.params(B, 1, H, D, Dv, 1, 64, 0, W, scale)
+        q_pos0 = n_ent - Q  # m = 1: query t sees entries 0..t
+        raw = rng.standard_normal((B, W + Q + 3, D))
+        raw_pos0 = q_pos0 + Q - raw.shape[1]
+        traw = to_bf(raw)
+        csa.hca(p, tq, csa.rows(tkv), csa.rows(traw), raw_pos0, q_pos0, N, out)
+    else:
+        idx = np.full((B, Q, k), -1, dtype=np.int32)
+        for b in range(B):
+            for i in range(Q):
+                sel = np.sort(rng.choice(N, size=k - 40, replace=False))
+                if i == 1:
+                    sel = sel[::-1]
+                row = np.concatenate([sel[:150], -np.ones(40, dtype=np.int64), sel[150:]])
+                idx[b, i, :row.size] = row
+        tidx = torch.from_numpy(idx).to(cuda_device)
+        csa.attend(p, tq, csa.rows(tkv), csa.rows(traw), raw_pos0, tidx, q_pos0, N, out)
+    torch.cuda.synchronize()
+    csa.device_status()
+    got = f64(out)
+    for b in range(B):
+        qv, kvv, rawv = f64(tq[b]), f64(tkv[b]), f64(traw[b])
+        pos = q_pos0 + np.arange(Q)
+        if dense:
+            ref = O.hca_attend(qv, kvv, rawv, raw_pos0, pos, 1, W, Dv, scale)
+        else:
+            ref = O.csa_attend(qv, kvv, rawv, raw_pos0, idx[b], pos, W, Dv, scale)
+        check_out(got[b], ref, False)
