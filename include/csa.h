@@ -163,6 +163,31 @@ int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, in
              int32_t* idx, void* ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
+ * csa_topk_noalloc -- csa_topk for callers that cannot allocate device memory
+ * at the point of the call (for instance code inside a host framework that
+ * owns every device allocation, or a path that must not call cudaMalloc
+ * because it can synchronise the device).  The pages have no counterpart of
+ * this call: it is a convenience of this library.
+ *
+ * Same arguments, results and errors as csa_topk, without the workspace: the
+ * scratch lives in one static device array of CSA_TOPK_NOALLOC_MAX_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The call allocates and frees nothing.
+ *   - Sizes whose scratch (csa_workspace_size(p, CSA_WS_TOPK, Q, N)) exceeds
+ *     CSA_TOPK_NOALLOC_MAX_BYTES are rejected with CSA_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (it must be the current device); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and the call re-zeroes what must start
+ *     at zero, but calls that overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ */
+#define CSA_TOPK_NOALLOC_MAX_BYTES (16u << 20)
+
+int csa_topk_noalloc(const csa_params* p, const float* scores, int64_t q_pos0, int Q, int64_t N,
+                     int32_t* idx, csa_stream_t stream);
+
+/*
  * csa_attend -- shared-KV (MQA) attention of every query head over the
  * selected entries plus the raw window ([csdn] "保留一小段最近距离的原始 KV
  * （滑动窗口）…注意力用共享 KV 的 MQA 形式"; [yudong] 2.2 Step 4):

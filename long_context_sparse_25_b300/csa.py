@@ -72,6 +72,7 @@ _SIGS = {
     "hca_attend": [C.POINTER(Params), _P, _I, C.POINTER(Rows), C.POINTER(Rows), _I64, _I64, _I,
                    _I64, _P, _I, _P, _SZ, _P],
     "csa_forward": [C.POINTER(Params), C.POINTER(ForwardArgs), _P, _SZ, _P],
+    "csa_topk_noalloc": [C.POINTER(Params), _P, _I64, _I, _I64, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -167,6 +168,16 @@ def topk(p: Params, scores, q_pos0, idx, ws=None, stream=None):
         ws = _workspace(nbytes, scores.device)
     _check(lib.csa_topk(C.byref(p), _ptr(scores), q_pos0, Q, N, _ptr(idx), _ptr(ws),
                         0 if ws is None else ws.numel(), _stream(stream)))
+
+
+TOPK_NOALLOC_MAX_BYTES = 16 << 20  # CSA_TOPK_NOALLOC_MAX_BYTES of include/csa.h
+
+
+def topk_noalloc(p: Params, scores, q_pos0, idx, stream=None):
+    """csa_topk_noalloc: top-k with the library's static scratch (no workspace)."""
+    B, Q, N = scores.shape
+    _check(lib.csa_topk_noalloc(C.byref(p), _ptr(scores), q_pos0, Q, N, _ptr(idx),
+                                _stream(stream)))
 
 
 def attend(p: Params, q, kv: Rows, raw: Rows | None, raw_pos0, idx, q_pos0, N, out, ws=None,

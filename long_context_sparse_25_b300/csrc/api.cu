@@ -3,6 +3,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 using namespace csa;
@@ -206,6 +208,65 @@ int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, in
   }
   return cuda_status(launch_topk(*p, scores, q_pos0, Q, N, idx, ws, (cudaStream_t)stream),
                      "csa_topk");
+}
+
+// ---------------------------------------------------------------------------
+// csa_topk_noalloc: csa_topk with its scratch in a fixed buffer of this
+// library instead of a caller workspace.  It is meant for callers that cannot
+// obtain device memory at the point of the call: code embedded in a host
+// framework that owns every device allocation, or paths that must not call
+// cudaMalloc because it can synchronise the device.  The buffer is a
+// file-scope device array, so every GPU that loads the library holds it
+// until the process exits.  Host code only sees a host-side stand-in for
+// the array's name, so its device address is looked up once per device, with
+// that device current, and handed to the kernels.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_topk_noalloc_scratch[CSA_TOPK_NOALLOC_MAX_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "csa_topk_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(CSA_ERR_UNSUPPORTED, "csa_topk_noalloc: device %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_topk_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e, "csa_topk_noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" int csa_topk_noalloc(const csa_params* p, const float* scores, int64_t q_pos0, int Q,
+                                int64_t N, int32_t* idx, csa_stream_t stream) {
+  CHECK(check_params(p, false, true));
+  CHECK(check_positions(q_pos0, Q, N, p->m));
+  if (Q == 0) return ok();
+  CHECK_PTR(idx);
+  if (N > 0) CHECK_PTR(scores);
+  REQUIRE(N <= 0x7fffffffLL, CSA_ERR_UNSUPPORTED, "N too large for int32 indices");
+  const size_t need = topk_workspace(*p, Q, N);
+  REQUIRE(need <= (size_t)CSA_TOPK_NOALLOC_MAX_BYTES, CSA_ERR_WORKSPACE,
+          "csa_topk_noalloc: these sizes need %zu bytes of scratch, the static buffer holds %zu "
+          "(use csa_topk with a workspace)",
+          need, (size_t)CSA_TOPK_NOALLOC_MAX_BYTES);
+  void* ws = nullptr;
+  if (need) CHECK(noalloc_scratch(&ws));
+  return cuda_status(launch_topk(*p, scores, q_pos0, Q, N, idx, ws, (cudaStream_t)stream),
+                     "csa_topk_noalloc");
 }
 
 static int attend_common(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_rows* kv,
