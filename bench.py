@@ -1,11 +1,11 @@
 #!/usr/bin/env python
-"""CSA decode at 1M-token context on one B300: tokens/s, with the roofline
-fraction of the dominant kernel (the lightning-indexer stream over the
-compressed-key cache).
+"""CSA on one B300: decode tokens/s at 1M-token context (the headline value)
+and prefill query-tokens/s at 64K tokens, each with the roofline fraction of
+its dominant kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Workload (default ``csa_decode_1m``): 32 sequences, one new token each at
+Headline workload (``csa_decode_1m``): 32 sequences, one new token each at
 position 2^20 - 1, 262,144 compressed entries per sequence (576-wide bf16 KV
 entries, 128-wide bf16 indexer keys), 64 indexer heads, top-1024, 128 query
 heads sharing the KV, raw window 128.  A step is the whole CSA path for that
@@ -14,9 +14,15 @@ score all entries, keep the top 1024, attend over them plus the window.  The
 caches (12 GB) are resident; each step streams 2.2 GB, far more than the
 126 MB L2, so no L2 flush is needed between steps.
 
+Second line of the same JSON object (``prefill``): ``csa_prefill_64k``, one
+65,536-token sequence, every query causal: compress 16,384 entries and keys,
+score the 5.4e8 visible (query, entry) pairs, keep the top 1024 per query,
+attend over them plus 128 window tokens.  Its 9.7 GB query tensor and 4.3 GB
+score matrix are far larger than L2.
+
 With --gpus N > 1 (torchrun, one process per GPU) every rank runs its own
-32-sequence batch (replicas, weak scaling; no collective on the data path) and
-the time is the max over ranks.
+batch (replicas, weak scaling; no collective on the data path) and the time
+is the max over ranks.
 
 --impl reference times the CPU oracle (float64 numpy) on the host cores over
 a bounded sample of the same workload: each step is the complete decode step
@@ -26,9 +32,8 @@ of one sequence.
 from __future__ import annotations
 
 import argparse
-import hashlib
+import gc
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -40,15 +45,15 @@ import torch
 
 ROOT = Path(__file__).resolve().parent
 METRIC = "CSA decode tok/s & prefill query-tok/s at 1M ctx; % of HBM/tensor roofline"
-FALLBACK_HBM_GBS = 6400.0
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
 def _peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
         d = json.loads(p.read_text())
-        return d.get("hbm_gbs", FALLBACK_HBM_GBS), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return {k: d.get(k, v) for k, v in FALLBACK.items()}, "measured"
+    return dict(FALLBACK), "fallback"
 
 
 def _blas_threads() -> int:
@@ -125,11 +130,16 @@ def run_reference(args, wl):
 
 # ---------------------------------------------------------------- GPU arm
 def _config(wl):
-    return {"workload": f"{wl.name}: CSA decode, B={wl.B}, context {wl.L} tokens "
-                        f"({wl.N} entries), k={wl.k}, H={wl.H}, D={wl.D_v}+{wl.D_qk - wl.D_v}, "
-                        f"indexer {wl.H_I}x{wl.d_I}, window {wl.W}, bf16",
-            "B": wl.B, "context": wl.L, "entries": wl.N, "k": wl.k,
-            "l2": "inputs larger than L2 (2.2 GB streamed per step > 126 MB), no flush"}
+    kind = "CSA decode" if wl.mode == "csa_decode" else wl.mode.replace("_", " ")
+    cfg = {"workload": f"{wl.name}: {kind}, B={wl.B}, context {wl.L} tokens ({wl.N} entries), "
+                       f"Q={wl.Q} per sequence, k={wl.k}, H={wl.H}, D={wl.D_v}+{wl.D_qk - wl.D_v}, "
+                       f"indexer {wl.H_I}x{wl.d_I}, window {wl.W}, {wl.dtype}",
+           "B": wl.B, "context": wl.L, "entries": wl.N, "queries_per_seq": wl.Q, "k": wl.k}
+    if wl.mode == "csa_decode":
+        cfg["l2"] = "inputs larger than L2 (2.2 GB streamed per step > 126 MB), no flush"
+    else:
+        cfg["l2"] = "inputs larger than L2 (9.7 GB of queries, 4.3 GB of scores per step), no flush"
+    return cfg
 
 
 class Clocks:
@@ -185,13 +195,15 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def _traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernel source changed since those counters were taken."""
+def _traffic(name: str):
+    """DRAM bytes per launch of kernel `name` from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel's source changed since
+    those counters were taken."""
+    import hashlib
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None
-    d = json.loads(p.read_text()).get(kernel)
+    d = json.loads(p.read_text()).get(name)
     if not d:
         return None
     src = ROOT / d["source"]
@@ -200,36 +212,54 @@ def _traffic(kernel: str):
     return d["bytes_per_launch"]
 
 
-def run_ours(args, wl):
+def algorithmic_work(wl):
+    """Algorithmic bytes (HBM-bound parts) and flops (tensor parts) of one step,
+    per part, from the method's definition (not from what a kernel does)."""
+    import numpy as np
+    B, N, m = wl.B, wl.N, wl.m
+    t = wl.q_pos0 + np.arange(wl.Q, dtype=np.int64)
+    nv = np.minimum((t + 1) // m, N)
+    win = np.minimum(wl.W, t + 1)
+    esz = 2
+    w = {}
+    if wl.mode.startswith("csa"):
+        new = N - (N - 1 if wl.mode.endswith("decode") else 0)
+        # raw rows + gates in, entries out, for the KV and the indexer keys
+        w["compress_bytes"] = B * new * (m * 2 * (wl.D_qk + wl.d_I) * esz + (wl.D_qk + wl.d_I) * esz)
+        w["index_bytes"] = B * (N * wl.d_I * esz + wl.Q * (wl.H_I * wl.d_I * esz + wl.H_I * 4))
+        w["index_flops"] = float(B * nv.sum() * wl.H_I * wl.d_I * 2)
+        keys = np.minimum(wl.k, nv) + win
+        w["attend_flops"] = float(B * keys.sum() * wl.H * (wl.D_qk + wl.D_v) * 2)
+        w["attend_bytes"] = B * (keys.sum() * wl.D_qk * esz
+                                 + wl.Q * wl.H * (wl.D_qk + wl.D_v) * esz)
+    return w
+
+
+def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
+            with_clocks=True):
+    """Time one workload: the whole step as a CUDA graph, each part in a graph
+    of its own, and the end-to-end path with host copies."""
     from long_context_sparse_25_b300 import csa, synth
     from long_context_sparse_25_b300.pipeline import Step
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
 
     inp = synth.make_inputs(wl, dev)
     step = Step(wl, inp)
     stream = torch.cuda.Stream(device=dev)
     p = step.p
     N = wl.N
+    decode = wl.mode.endswith("decode")
+    n0 = N - 1 if decode else 0
     scores, sel = step.scores(), step.selected()
     off = sel.data_ptr() - step.ws.data_ptr() + sel.numel() * 4
     off = (off + 255) // 256 * 256
     rest = step.ws[off:]
 
     # the step's C-ABI calls one by one (the kernels csa_forward launches),
-    # used to time each part in a graph of its own
+    # each timed in a graph of its own
     parts = {
-        "compress": lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, N - 1, N, step.kv,
+        "compress": lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, n0, N, step.kv,
                                           x_pos0=wl.raw_pos0, stream=stream),
-                             csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, N - 1, N,
+                             csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, n0, N,
                                           step.keys, x_pos0=wl.raw_pos0, stream=stream)),
         "index": lambda: csa.index(p, inp["q_idx"], inp["w"], step.keys, wl.q_pos0, N, scores,
                                    q_scale=inp.get("q_idx_scale"), stream=stream),
@@ -237,6 +267,8 @@ def run_ours(args, wl):
         "attend": lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0,
                                      N, step.out, ws=rest, stream=stream),
     }
+    if not parts_wanted:
+        parts = {}
     with torch.cuda.stream(stream):
         for _ in range(2):
             step.run(stream=stream)
@@ -265,46 +297,40 @@ def run_ours(args, wl):
                 a_.record(stream)
                 graph.replay()
                 b_.record(stream)
-        return evs
+        torch.cuda.synchronize()
+        return sum(a_.elapsed_time(b_) for a_, b_ in evs)
 
-    clocks = Clocks() if rank == 0 else None
+    clocks = Clocks() if (rank == 0 and with_clocks) else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    ev = timed(g_full, args.steps)
-    torch.cuda.synchronize()
+    total_ms = timed(g_full, args.steps)
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    total_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    ms = total_ms / args.steps
-    value = wl.B * world / (ms / 1e3)
+    ms = float(t.item()) / args.steps
     csa.device_status(stream)
 
-    # each part on its own (same kernels, same data), for the roofline and
-    # the breakdown
-    per_kernel = {}
-    for name, g_ in g_part.items():
-        evs = timed(g_, args.steps)
-        torch.cuda.synchronize()
-        per_kernel[name] = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
+    per_part = {name: timed(g_, args.steps) / args.steps for name, g_ in g_part.items()}
 
     # end to end: the step's new inputs from pinned host memory, the output back
     h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi")]
+    if "q_idx_scale" in inp:
+        h2d.append(inp["q_idx_scale"])
     host_in = [t_.cpu().pin_memory() for t_ in h2d]
     host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
     bi = sum(t_.numel() * t_.element_size() for t_ in h2d)
     bo = host_out.numel() * host_out.element_size()
+    ne = e2e_steps or args.steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for it in range(args.steps + 2):
+        for it in range(ne + 2):
             if it == 2:
                 e0.record(stream)
             for d_, h_ in zip(h2d, host_in):
@@ -313,24 +339,77 @@ def run_ours(args, wl):
             host_out.copy_(step.out, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    te = torch.tensor([e0.elapsed_time(e1) / ne], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(te, op=dist.ReduceOp.MAX)
     e2e_ms = float(te.item())
+    units = wl.B * wl.Q * world
+    res = {"ms": ms, "value": units / (ms / 1e3), "per_part_ms": per_part, "clocks": clk,
+           "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
+                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+           "launches_per_step": step.launches_per_step()}
+    del step, inp, g_full, g_part, host_in, host_out
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
+def roofline(wl, per_part, peaks, peak_kind):
+    """Roofline of the dominant part: HBM for the decode indexer stream, the
+    bf16 tensor peak for the prefill contractions (parts timed alone, so the
+    burst peak applies)."""
+    w = algorithmic_work(wl)
+    if wl.mode == "csa_decode":
+        name = "index"
+        achieved = w["index_bytes"] / (per_part[name] / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s", "frac": achieved / peak,
+                "traffic": _traffic(f"index_tc_kernel:{wl.name}"),
+                "algorithmic_bytes_per_launch": w["index_bytes"]}
+    name = max(("index", "attend"), key=lambda k: per_part[k])
+    achieved = w[f"{name}_flops"] / (per_part[name] / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
+            "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": _traffic(f"{name}:{wl.name}"),
+            "algorithmic_flops_per_launch": w[f"{name}_flops"],
+            "other_part": {k: (w[f"{k}_flops"] / (per_part[k] / 1e3) / 1e12) / peak
+                           for k in ("index", "attend") if k != name}}
+
+
+def run_ours(args, wl):
+    from long_context_sparse_25_b300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_kind = _peaks()
+
+    head = measure(args, wl, dev, dist, world, rank)
+    prefill = None
+    if not args.no_prefill and wl.mode == "csa_decode":
+        pw = synth.WORKLOADS["csa_prefill_64k"]
+        pr = measure(args, pw, dev, dist, world, rank, e2e_steps=min(args.steps, 5),
+                     with_clocks=False)
+        prefill = {"workload": _config(pw)["workload"], "value": pr["value"],
+                   "unit": "query-tok/s", "ms_per_step": pr["ms"],
+                   "per_part_ms": pr["per_part_ms"],
+                   "roofline": roofline(pw, pr["per_part_ms"], peaks, peak_kind),
+                   "e2e": pr["e2e"], "gpu_launches": pr["launches_per_step"] * args.steps}
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
-
-    # roofline of the dominant kernel: the indexer's stream over the key cache
-    peak, peak_kind = _peaks()
-    idx_bytes = wl.B * (N * wl.d_I * 2 + wl.H_I * wl.d_I * 2 + wl.H_I * 4)
-    idx_ms = per_kernel["index"]
-    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and wl.mode == "csa_decode":
         nseq = 2
         cinp = _cpu_inputs(wl, nseq)
         t0 = time.perf_counter()
@@ -338,24 +417,23 @@ def run_ours(args, wl):
             _oracle_decode_step(wl, cinp, b)
         sec = time.perf_counter() - t0
         cpu = {"value": nseq / sec, "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
-               "sample": f"{nseq} of {wl.B} sequences, complete decode step each"}
-    launches_per_step = step.launches_per_step()
+               "sample": f"{nseq} of {wl.B} sequences, complete decode step each "
+                         f"(compress tail, index {wl.N} entries, top-{wl.k}, attend)"}
+    decode = wl.mode.endswith("decode")
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(wl),
-        "roofline": {"bound": "hbm", "kernel": "index", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": _traffic("index_decode"),
-                     "algorithmic_bytes_per_launch": idx_bytes},
-        "per_part_ms": per_kernel,
+        "metric": METRIC, "value": head["value"], "unit": "tok/s" if decode else "query-tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(wl),
+        "roofline": roofline(wl, head["per_part_ms"], peaks, peak_kind),
+        "per_part_ms": head["per_part_ms"],
         "timing": "CUDA graph of the whole step replayed per timed step; CUDA events on the "
-                  "launching stream; the indexer timed alone in its own graph for the roofline",
-        "e2e": {"value": wl.B * world / (e2e_ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+                  "launching stream; each part timed alone in a graph of its own for the roofline",
+        "e2e": head["e2e"],
+        "gpu_launches": head["launches_per_step"] * args.steps,
+        "clocks": head["clocks"],
         "cpu_baseline": cpu,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -370,9 +448,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="csa_decode_1m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the 64K-token prefill measurement")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiler captures)")
+    ap.add_argument("--context", type=int, default=None,
+                    help="override the workload's context length (a prefill keeps every query)")
     args = ap.parse_args()
     from long_context_sparse_25_b300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(B=args.batch)
+    if args.context:
+        wl = wl.replace(L=args.context, Q=args.context if wl.mode == "csa_prefill" else wl.Q)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

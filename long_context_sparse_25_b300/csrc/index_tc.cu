@@ -74,6 +74,11 @@ struct Sched {
     if (args.mode == 0) {
       t = args.total * cta / grid;
       t_end = args.total * (cta + 1) / grid;
+      // position of tile t, then walked forward without divisions
+      const int64_t per_b = (int64_t)args.nQB * args.tps;
+      b = (int)(t / per_b);
+      qb = (int)((t / args.tps) % args.nQB);
+      kt = (int)(t % args.tps);
     } else {
       r = 0;
       kt = 0;
@@ -84,11 +89,17 @@ struct Sched {
   __device__ bool next(int& ob, int& oqb, int& okt) {
     if (a->mode == 0) {
       if (t >= t_end) return false;
-      const int64_t per_b = (int64_t)a->nQB * a->tps;
-      ob = (int)(t / per_b);
-      oqb = (int)((t / a->tps) % a->nQB);
-      okt = (int)(t % a->tps);
+      ob = b;
+      oqb = qb;
+      okt = kt;
       ++t;
+      if (++kt == a->tps) {
+        kt = 0;
+        if (++qb == a->nQB) {
+          qb = 0;
+          ++b;
+        }
+      }
       return true;
     }
     while (kt >= kt_end) {
@@ -127,6 +138,9 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  // [epilogue warps][QPW * H_I], read as float4: 16-byte aligned
+  float* a_w_smem = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~(uintptr_t)15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NM = a.NQ * a.H_I;  // MMA N
@@ -240,8 +254,28 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const int QPW = a.NQ / kEpiWG;  // queries per warpgroup
+    // this warp's copy of the head weights of its QPW queries (per-warp, so
+    // no barrier across warps is needed)
+    float* sw = a_w_smem + (size_t)ew * QPW * a.H_I;
     uint32_t acc_it = 0;
+    int cur_b = -1, cur_qb = -1;
     while (sch.next(b, qb, kt)) {
+      if (b != cur_b || qb != cur_qb) {
+        // stage w (times the e4m3 query-row scale) once per query block
+        __syncwarp();
+        for (int e = lane; e < QPW * a.H_I; e += 32) {
+          const int ql = e / a.H_I, j = e - ql * a.H_I;
+          int i = qb * a.NQ + wg * QPW + ql;
+          if (i >= a.Q) i = a.Q - 1;
+          const int64_t wi = ((int64_t)b * a.Q + i) * a.H_I + j;
+          float wj = __ldg(a.w + wi);
+          if (kFP8) wj *= __ldg(a.q_scale + wi);
+          sw[e] = wj;
+        }
+        __syncwarp();
+        cur_b = b;
+        cur_qb = qb;
+      }
       const uint32_t acc = acc_it & 1;
       // one lane waits, the warp follows converged (tcgen05.ld is .sync.aligned)
       int okw = lane == 0 ? (int)tc::mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, err, 6) : 0;
@@ -252,22 +286,35 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       float sc[4];
       for (int ql = 0; ql < QPW; ++ql) {
         const int qi = wg * QPW + ql;
-        const int i = qb * a.NQ + qi;
-        float acc_s = 0.f;
         const uint32_t col = acc * NM + qi * a.H_I;
-        const int64_t wrow = ((int64_t)b * a.Q + (i < a.Q ? i : a.Q - 1)) * a.H_I;
-        for (int j0 = 0; j0 < a.H_I; j0 += 32) {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col + j0, r);
+        const float4* wq = reinterpret_cast<const float4*>(sw + ql * a.H_I);
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < a.H_I; j0 += 64) {
+          uint32_t r0[32], r1[32];
+          const bool two = j0 + 32 < a.H_I;
+          tc::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col + j0, r0);
+          if (two) tc::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col + j0 + 32, r1);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            float wj = __ldg(a.w + wrow + j0 + jj);
-            if (kFP8) wj *= __ldg(a.q_scale + wrow + j0 + jj);
-            acc_s = fmaf(wj, fmaxf(__uint_as_float(r[jj]), 0.f), acc_s);
+          for (int v = 0; v < 8; ++v) {
+            const float4 w4 = wq[j0 / 4 + v];
+            part[0] = fmaf(w4.x, fmaxf(__uint_as_float(r0[4 * v + 0]), 0.f), part[0]);
+            part[1] = fmaf(w4.y, fmaxf(__uint_as_float(r0[4 * v + 1]), 0.f), part[1]);
+            part[2] = fmaf(w4.z, fmaxf(__uint_as_float(r0[4 * v + 2]), 0.f), part[2]);
+            part[3] = fmaf(w4.w, fmaxf(__uint_as_float(r0[4 * v + 3]), 0.f), part[3]);
+          }
+          if (two) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 w4 = wq[j0 / 4 + 8 + v];
+              part[0] = fmaf(w4.x, fmaxf(__uint_as_float(r1[4 * v + 0]), 0.f), part[0]);
+              part[1] = fmaf(w4.y, fmaxf(__uint_as_float(r1[4 * v + 1]), 0.f), part[1]);
+              part[2] = fmaf(w4.z, fmaxf(__uint_as_float(r1[4 * v + 2]), 0.f), part[2]);
+              part[3] = fmaf(w4.w, fmaxf(__uint_as_float(r1[4 * v + 3]), 0.f), part[3]);
+            }
           }
         }
-        sc[ql] = acc_s;
+        sc[ql] = (part[0] + part[1]) + (part[2] + part[3]);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -429,7 +476,8 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   if (a.total < grid) grid = a.total;
   if (grid < 1) grid = 1;
   const size_t smem = 1024 + (size_t)a.stages * a.a_bytes + (size_t)a.nb * a.b_bytes +
-                      (2 * a.stages + 9) * sizeof(uint64_t) + 16;
+                      (2 * a.stages + 9) * sizeof(uint64_t) + 16 + 16 +
+                      (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
   const int threads = 64 + 128 * epi_wg;
   cudaError_t e;
 #define CSA_LAUNCH_TC(FP8, EW)                                                                  \

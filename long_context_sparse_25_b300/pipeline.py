@@ -75,13 +75,27 @@ class Step:
         return self.ws[off: off + n * 4].view(torch.int32).view(wl.B, wl.Q, wl.k)
 
     def launches_per_step(self) -> int:
-        """Kernels one run() launches (as the library's launch plan stands)."""
+        """Kernels one run() launches, following the library's launch plan:
+        compress (one per cache), the indexer, top-k (three kernels for a few
+        long rows, one otherwise), attention (the tensor-core kernel for bf16 /
+        mixed caches with 128 heads, plus a combine kernel when a decode query
+        is split; the CUDA-core kernel plus a combine when its rows are split)."""
         wl = self.wl
-        attend = 1 + (1 if csa.workspace_size(self.p, csa.WS_HCA if wl.mode.startswith("hca")
-                                              else csa.WS_ATTEND, wl.Q, wl.N) else 0)
+        rows = wl.B * wl.Q
+        tc = wl.dtype != "f32" and wl.H == 128
+        if wl.mode.startswith("hca"):
+            kd = min((wl.q_pos0 + wl.Q) // wl.m, wl.N)
+        else:
+            kd = wl.k
+        n_keys = ((kd + 3) // 4) * 4 + wl.W
+        if tc:
+            attend = 1 + (1 if (wl.Q == 1 and n_keys > 128) else 0)
+        else:
+            attend = 1 + (1 if (rows < 1024 and kd + wl.W > 128) else 0)
         if wl.mode.startswith("hca"):
             return 1 + attend
-        return 2 + 1 + csa.topk_launches(self.p, wl.Q, wl.N) + attend
+        topk = 3 if (wl.N > 16384 and wl.k <= 4096 and rows < 256) else 1
+        return 2 + 1 + topk + attend
 
     def run(self, stream=None):
         wl = self.wl

@@ -72,3 +72,34 @@ def _decode_parity(wl, dev, attn_seqs):
 def test_decode_1m_full_size(cuda_device):
     wl = synth.WORKLOADS["csa_decode_1m"]
     _decode_parity(wl, cuda_device, attn_seqs={0, 5, 11, 16, 21, 26, 30, 31})
+
+
+def test_prefill_64k_full_size(cuda_device):
+    """CSA prefill at 65,536 tokens (16,384 entries, k = 1024, 128 heads), in
+    the launch configuration bench.py times (one csa_forward): every
+    compressed entry and indexer key bit-exact; scores, selection and
+    attention output on a fixed query sample (the first 128 queries, every
+    256th, the last 128)."""
+    wl = synth.WORKLOADS["csa_prefill_64k"]
+    dev = cuda_device
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    m, N = wl.m, wl.N
+    qs = np.unique(np.concatenate([np.arange(128), np.arange(0, wl.Q, 256),
+                                   np.arange(wl.Q - 128, wl.Q)]))
+    x, g = f64(inp["x"][0]), f64(inp["g"][0])
+    xi, gi = f64(inp["xi"][0]), f64(inp["gi"][0])
+    kv = O.store_rows(O.compress(x, g, f64(inp["bias"]), m), "bf16")
+    keys = O.store_rows(O.compress(xi, gi, f64(inp["bias_i"]), m), "bf16")
+    assert np.array_equal(f64(step.kv_buf[0]), kv), "compressed entries differ"
+    assert np.array_equal(f64(step.keys_buf[0]), keys), "indexer keys differ"
+    pos = wl.q_pos0 + qs
+    tq = torch.from_numpy(qs).to(dev).long()
+    ref = O.index_scores(f64(inp["q_idx"][0][tq]), f64(inp["w"][0][tq]), keys, pos, m)
+    check_scores(step.scores()[0][tq].cpu().double().numpy(), ref)
+    sel = step.selected()[0][tq].cpu().numpy()
+    check_selection(sel, ref, O.n_vis(pos, m), wl.k)
+    o = O.csa_attend(f64(inp["q"][0][tq]), kv, x, wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)
+    check_out(f64(step.out[0][tq]), o, False)
