@@ -20,20 +20,25 @@
 // the softmax reads S it writes P (bf16 pairs) over the first 64 columns of
 // the same buffer, and P . V runs with A taken from TMEM.
 //
-// Shared memory: Q of the query (D_qk/64 chunks of 128 x 64 bf16, resident)
-// and a ring of kRing chunks of 128 keys x 64 dims.  For every tile of 128
-// keys the producer gathers the D_qk/64 chunks of the keys (TMA gather4 of
-// four rows at a time) and then, one tile later, the D_v/128 chunks of the
-// value half.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims
-// in bf16) are converted by the producer warp itself: for QK^T each
-// dequantised key is split exactly into a bf16 high part and a bf16 low part
-// (two chunk loads per nope chunk, both multiplied by the same Q chunk), so
-// the scores see the key to about 2^-17; for PV the chunk holds the codes
-// themselves (exact in bf16) and the row scale is folded into P, which is
-// split the same way (PV runs on the high and on the low part).  The
-// MMA order is S(0), S(1), PV(0), S(2), PV(1), ... so the softmax of tile u
-// overlaps S(u+1).  A key row doubles as its value row: the same 128-byte
-// swizzled chunk is K-major for QK^T and MN-major for PV.
+// Shared memory: Q of the query (D_qk/64 chunks of 128 x 64 bf16, loaded once
+// by TMA and resident) and a ring of kRing chunks of 128 keys x 64 dims.  For
+// every tile of 128 keys three producer warps gather the D_qk/64 chunks of the
+// keys and then, one tile later, the D_v/128 chunks of the value half, with
+// 16-byte cp.async copies: each lane computes its own gathered row address
+// and swizzled destination (TMA gathers take their operands from warp-uniform
+// registers, so 32 lanes with 32 different rows serialise).  A thread keeps
+// kInFlight chunks in flight; once one has landed it issues a proxy fence
+// (its writes become visible to the tensor cores) and arrives on the chunk's
+// barrier.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims in
+// bf16) are converted by the producers themselves: for QK^T each dequantised
+// key is split exactly into a bf16 high part and a bf16 low part (two chunk
+// loads per nope chunk, both multiplied by the same Q chunk), so the scores
+// see the key to about 2^-17; for PV the chunk holds the codes themselves
+// (exact in bf16) and the row scale is folded into P, which is split the same
+// way (PV runs on the high and on the low part).  The MMA order is S(0),
+// S(1), PV(0), S(2), PV(1), ... so the softmax of tile u overlaps S(u+1).  A
+// key row doubles as its value row: the same 128-byte swizzled chunk is
+// K-major for QK^T and MN-major for PV.
 //
 // Softmax: one thread per head row, log2 domain, running maximum updated only
 // when a tile's maximum exceeds it by more than 2^8 (then O and the running
@@ -43,8 +48,8 @@
 // tiles (chosen from the key-list length only, never from the batch) and
 // merges the splits in order in attend_tc_combine_kernel.
 //
-// Roles: warp 0 producer, warp 1 TMEM allocator + MMA issuer (one thread),
-// warps 2-5 softmax / rescale / epilogue.  Every mbarrier wait is bounded; a
+// Roles: warps 0-2 producers, warp 3 TMEM allocator + MMA issuer (one
+// thread), warps 4-7 softmax / rescale / epilogue.  Every mbarrier wait is bounded; a
 // timeout is recorded in a device error word and the kernel returns.
 #include <cudaTypedefs.h>
 
@@ -62,7 +67,12 @@ constexpr int kRing = 5;             // key chunk slots
 constexpr uint32_t kChunk = 16384;   // 128 rows x 128 bytes
 constexpr int kMaxQChunks = 9;       // D_qk <= 576
 constexpr float kRescaleLog2 = 8.f;  // rescale when the maximum grows by more than 2^8
-constexpr int kThreads = 192;
+constexpr int kProdWarps = 3;        // warps 0-2: key-chunk producers (cp.async)
+constexpr int kProd = kProdWarps * 32;
+constexpr int kUnits = (kChunk / 16 + kProd - 1) / kProd;  // 16-byte units per producer thread
+constexpr int kMmaWarp = 3;          // warp 3: TMEM allocator + MMA issuer
+constexpr int kThreads = 256;        // + warps 4-7: softmax / epilogue
+constexpr int kInFlight = 3;         // cp.async chunk groups a producer thread keeps in flight
 
 struct AttArgs {
   int B, Q, H, D_qk, D_v, k, W, m;
@@ -75,6 +85,7 @@ struct AttArgs {
   int64_t N, kv_rows, raw_rows, raw_pos0, q_pos0;
   float c_log2;  // scale * log2(e)
   const int32_t* idx;
+  const uint16_t* kv16;  // bf16 entries: [B, kv_rows, D_qk]
   const uint8_t* codes;  // e4m3 entries: [B, kv_rows, nope]
   const uint16_t* rope;  // [B, kv_rows, D_qk - nope]
   const float* kscale;   // [B, kv_rows]
@@ -110,49 +121,42 @@ __device__ __forceinline__ KeyList key_list(const AttArgs& a, int i) {
   return kl;
 }
 
-// Rows of the four key slots j0..j0+3 (j0 % 4 == 0): entry rows index the
-// entry cache, window rows the raw rows; invalid slots point at a valid row
-// and are masked in the softmax.
-struct Group {
-  int rows[4];
-  int win;       // 1: rows of the raw-row tensor
-  uint32_t vmask;  // bit q: slot j0+q holds a key
+// Source row of key slot j of a query's list: an entry row (entry cache) or
+// a window row (raw rows).  Empty slots point at a valid row of the same
+// kind and are masked in the softmax.
+struct SlotSrc {
+  int64_t row;  // row index into the entry cache or into the raw rows
+  bool win;
+  bool valid;
 };
 
-__device__ __forceinline__ Group group_rows(const AttArgs& a, const KeyList& kl, int b,
-                                            int64_t qrow, int j0) {
-  Group g;
-  g.vmask = 0;
-  if (j0 < kl.k_ent || a.W == 0) {
-    g.win = 0;
-    for (int q = 0; q < 4; ++q) {
-      const int j = j0 + q;
-      int64_t e = 0;
-      bool v = false;
-      if (j < kl.kd) {
-        if (a.dense) {
-          e = j;
-          v = true;
-        } else {
-          e = a.idx[qrow * (int64_t)a.k + j];
-          v = e >= 0 && e < a.N;  // -1 (and anything out of range) is an empty slot
-          if (!v) e = 0;
-        }
+__device__ __forceinline__ SlotSrc slot_src(const AttArgs& a, const KeyList& kl, int b,
+                                            int64_t qrow, int j) {
+  SlotSrc r;
+  if (j < kl.k_ent || a.W == 0) {
+    int64_t e = 0;
+    bool v = false;
+    if (j < kl.kd) {
+      if (a.dense) {
+        e = j;
+        v = true;
+      } else {
+        e = a.idx[qrow * (int64_t)a.k + j];
+        v = e >= 0 && e < a.N;  // -1 (and anything out of range) is an empty slot
+        if (!v) e = 0;
       }
-      g.rows[q] = (int)((int64_t)b * a.kv_rows + e);
-      g.vmask |= (v ? 1u : 0u) << q;
     }
+    r.row = (int64_t)b * a.kv_rows + e;
+    r.win = false;
+    r.valid = v;
   } else {
-    g.win = 1;
-    const int w0 = j0 - kl.k_ent;
-    for (int q = 0; q < 4; ++q) {
-      const bool v = w0 + q < kl.w_len;
-      const int64_t pos = kl.lo + (v ? w0 + q : 0);
-      g.rows[q] = (int)((int64_t)b * a.raw_rows + (pos - a.raw_pos0));
-      g.vmask |= (v ? 1u : 0u) << q;
-    }
+    const int w = j - kl.k_ent;
+    r.valid = w < kl.w_len;
+    const int64_t pos = kl.lo + (r.valid ? w : 0);
+    r.row = (int64_t)b * a.raw_rows + (pos - a.raw_pos0);
+    r.win = true;
   }
-  return g;
+  return r;
 }
 
 // 16 bytes of a 128-byte swizzled row: unit u of row r of a chunk.
@@ -166,80 +170,62 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return l | (h << 16);
 }
 
-// Mixed-precision cache: one chunk of 128 key rows x 64 dims written by the
-// producer warp itself (lane l: slots 4l..4l+3), as bf16.
-//   kHi:  dequantised nope dims, rounded to bf16 (RoPE dims and window rows:
+// Mixed-precision cache: 16 bytes (8 dims, from dim c*64 + uc*8) of one key
+// row of a chunk, as bf16, written by a producer thread itself.
+//   kHi:  dequantised nope dims rounded to bf16 (RoPE dims and window rows:
 //         their bf16 values);
-//   kLo:  the rounding error of kHi, rounded to bf16 (window rows: 0);
+//   kLo:  the rounding error of kHi, rounded to bf16 (window rows, RoPE: 0);
 //   kVal: the e4m3 codes as bf16 (exact; the row scale goes into P), window
-//         rows as they are.
+//         and RoPE dims as they are.
 enum ChunkMode { kHi = 0, kLo = 1, kVal = 2 };
 
-__device__ void manual_chunk(const AttArgs& a, uint8_t* dst, const Group& g, int c, int mode) {
-  const int lane = threadIdx.x & 31;
-  for (int q = 0; q < 4; ++q) {
-    const int r = lane * 4 + q;
-    const int64_t row = g.rows[q];
-    uint4 v[8];
-    if (g.win) {
-      if (mode == kLo) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + c * 64);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u);
-      }
-    } else if (c * 64 < a.nope) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.codes + row * a.nope + c * 64);
-      const float sc = mode == kVal ? 1.f : __ldg(a.kscale + row);
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const uint4 cv = __ldg(src + u4);
-        const uint32_t w4[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t word = w4[h * 2 + e / 2];
-            const int sh = (e & 1) * 16;
-            // code * scale in fp32 is within 2^-24 of the exact product; the
-            // high part is its bf16 rounding, the low part the (exact) rest
-            float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * sc;
-            float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * sc;
-            if (mode == kLo) {
-              f0 -= __bfloat162float(__float2bfloat16_rn(f0));
-              f1 -= __bfloat162float(__float2bfloat16_rn(f1));
-            }
-            o[e] = pack_bf16(f0, f1);
-          }
-          v[u4 * 2 + h] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-    } else {
-      if (mode == kLo) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        const int rw = a.D_qk - a.nope;
-        const uint4* src =
-            reinterpret_cast<const uint4*>(a.rope + row * rw + (c * 64 - a.nope));
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(dst + swz(r, u)) = v[u];
+__device__ __forceinline__ uint4 manual_unit(const AttArgs& a, int64_t row, bool win, int c,
+                                             int uc, int mode) {
+  const int d0 = c * 64 + uc * 8;
+  if (win) {
+    if (mode == kLo) return make_uint4(0u, 0u, 0u, 0u);
+    return __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
   }
-  tc::fence_proxy_async_smem();
+  if (d0 >= a.nope) {
+    if (mode == kLo) return make_uint4(0u, 0u, 0u, 0u);
+    const int rw = a.D_qk - a.nope;
+    return __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
+  }
+  const uint2 cv = __ldg(reinterpret_cast<const uint2*>(a.codes + row * a.nope + d0));
+  const float sc = mode == kVal ? 1.f : __ldg(a.kscale + row);
+  const uint32_t w2[2] = {cv.x, cv.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t word = w2[e / 2];
+    const int sh = (e & 1) * 16;
+    // code * scale in fp32 is within 2^-24 of the exact product; the high
+    // part is its bf16 rounding, the low part the (exact) rest
+    float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * sc;
+    float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * sc;
+    if (mode == kLo) {
+      f0 -= __bfloat162float(__float2bfloat16_rn(f0));
+      f1 -= __bfloat162float(__float2bfloat16_rn(f1));
+    }
+    o[e] = pack_bf16(f0, f1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_kv,
-                     const __grid_constant__ CUtensorMap tm_raw, const AttArgs a) {
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -278,96 +264,154 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRing; ++s) {
-      tc::mbar_init(&ring_full[s], 1);
+      tc::mbar_init(&ring_full[s], kProdWarps * 32);  // every producer thread arrives
       tc::mbar_init(&ring_empty[s], 1);
     }
     tc::mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&s_full[s], 1);
       tc::mbar_init(&p_full[s], 4);
-      tc::mbar_init(&mask_full[s], 1);
+      tc::mbar_init(&mask_full[s], kProdWarps);
       tc::mbar_init(&mask_empty[s], 4);
     }
     tc::mbar_init(o_done, 1);
     tc::mbar_init(mma_done, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tm_q);
-    if (!kE4M3) tc::prefetch_tmap(&tm_kv);
-    if (a.W > 0 && !kE4M3) tc::prefetch_tmap(&tm_raw);
+
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, 512);
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && n > 0) {
-    // ------------------------------------------------------------ producer
-    bool ok = true;
-    if (lane == 0) {
-      tc::mbar_expect_tx(q_full, a.nc * kChunk);
-      for (int c = 0; c < a.nc; ++c)
-        tc::tma_load_2d(sQ + c * kChunk, &tm_q, q_full, c * 64, (int)(qrow * a.H));
-    }
-    uint32_t lt = 0;
-    auto load_chunk = [&](int c, int mode, const Group& g) -> bool {
-      const uint32_t slot = lt % kRing;
-      int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ring_empty[slot], ((lt / kRing) & 1) ^ 1, err, 11);
-      okw = __shfl_sync(0xffffffffu, okw, 0);
-      if (!okw) return false;
-      uint8_t* dst = sRing + slot * kChunk;
-      if (kE4M3) {
-        manual_chunk(a, dst, g, c, mode);
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&ring_full[slot]);
-      } else {
-        if (lane == 0) tc::mbar_expect_tx(&ring_full[slot], kChunk);
-        __syncwarp();
-        tc::tma_gather4(dst + lane * 512, g.win ? &tm_raw : &tm_kv, &ring_full[slot], c * 64,
-                        g.rows[0], g.rows[1], g.rows[2], g.rows[3]);
+  if (warp < kProdWarps) {
+    // ------------------------------------------------------------ producers
+    // Thread pt copies the 16-byte units pt + kProd*i of every chunk (unit u:
+    // row u/8, bytes 16*(u%8) of the row) with cp.async, each lane with its
+    // own gathered address, keeps kInFlight chunks in flight, and for each
+    // chunk that has landed makes its writes visible to the tensor cores
+    // (proxy fence) before arriving.
+    const int pt = threadIdx.x;
+    if (n > 0) {
+      if (pt == 0) {
+        tc::mbar_expect_tx(q_full, a.nc * kChunk);
+        for (int c = 0; c < a.nc; ++c)
+          tc::tma_load_2d(sQ + c * kChunk, &tm_q, q_full, c * 64, (int)(qrow * a.H));
       }
-      ++lt;
-      return true;
-    };
-    Group prev{};
-    for (int u = 0; u <= n && ok; ++u) {
-      Group cur{};
-      if (u < n) {
-        cur = group_rows(a, kl, b, qrow, (tile0 + u) * kT + lane * 4);
-        // validity ballots of the tile for the softmax
+      const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv16);
+      const uint8_t* rawb = reinterpret_cast<const uint8_t*>(a.raw16);
+      const int64_t rowb = (int64_t)a.D_qk * 2;
+      uint32_t lt = 0, pend = 0;
+      bool ok = true;
+      auto issue_chunk = [&](int c, int mode, const int64_t (&rr)[kUnits], uint32_t wb) -> bool {
+        const uint32_t slot = lt % kRing;
         int okw = 1;
-        if (lane == 0) okw = tc::mbar_wait(&mask_empty[u & 1], ((u >> 1) & 1) ^ 1, err, 12);
+        if (lane == 0) okw = tc::mbar_wait(&ring_empty[slot], ((lt / kRing) & 1) ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) break;
-        uint32_t bal[4];
+        if (!okw) return false;
+        const uint32_t dst = tc::smem_u32(sRing + slot * kChunk);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) bal[q] = __ballot_sync(0xffffffffu, (cur.vmask >> q) & 1);
-        if (lane < 4) smask[(u & 1) * 4 + lane] = bal[lane];
-        if (kE4M3) {
-          // scale of each slot's value row (1 for window rows and empty slots)
-          for (int q = 0; q < 4; ++q) {
-            float sc = 1.f;
-            if (!cur.win && ((cur.vmask >> q) & 1)) sc = __ldg(a.kscale + cur.rows[q]);
-            svscale[(u & 1) * 128 + lane * 4 + q] = sc;
+        for (int i = 0; i < kUnits; ++i) {
+          const int unit = pt + kProd * i;
+          if (unit < (int)(kChunk / 16)) {
+            const int r = unit >> 3, uc = unit & 7;
+            if (kE4M3) {
+              const uint4 v = manual_unit(a, rr[i], (wb >> i) & 1, c, uc, mode);
+              *reinterpret_cast<uint4*>(sRing + slot * kChunk + swz(r, uc)) = v;
+            } else {
+              const uint8_t* src = ((wb >> i) & 1 ? rawb : kvb) + rr[i] * rowb + c * 128 + uc * 16;
+              cp_async16(dst + swz(r, uc), src);
+            }
           }
         }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
-        for (int cc = 0; cc < a.nsc && ok; ++cc)
-          ok = cc < a.nc ? load_chunk(cc, kHi, cur) : load_chunk(cc - a.nc, kLo, cur);
+        if (kE4M3) {
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(&ring_full[slot]);
+        } else {
+          cp_async_commit();
+          if (++pend > (uint32_t)kInFlight) {
+            cp_async_wait<kInFlight>();
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&ring_full[(lt - kInFlight) % kRing]);
+            --pend;
+          }
+        }
+        ++lt;
+        return true;
+      };
+      // gathered rows of tile u's units, and the two mask slots of each thread
+      struct TileRows {
+        int64_t rr[kUnits];
+        uint32_t wb;
+        SlotSrc s0, s1;
+      };
+      const bool has1 = pt + kProd < kT;
+      auto tile_rows = [&](int u, TileRows& t) {
+        const int jt = (tile0 + u) * kT;
+        t.wb = 0;
+#pragma unroll
+        for (int i = 0; i < kUnits; ++i) {
+          const int unit = pt + kProd * i;
+          const int r = unit < (int)(kChunk / 16) ? unit >> 3 : 0;
+          const SlotSrc ss = slot_src(a, kl, b, qrow, jt + r);
+          t.rr[i] = ss.row;
+          t.wb |= (ss.win ? 1u : 0u) << i;
+        }
+        t.s0 = slot_src(a, kl, b, qrow, jt + pt);
+        t.s1 = slot_src(a, kl, b, qrow, jt + (has1 ? pt + kProd : pt));
+      };
+      TileRows cur, nxt, prev;
+      tile_rows(0, cur);
+      for (int u = 0; u <= n && ok; ++u) {
+        if (u < n) {
+          // validity of slots pt and pt + 96 (and, for mixed caches, the scale
+          // of their value rows) for the softmax: ballot word w covers slots
+          // 32w .. 32w+31
+          int okw = 1;
+          if (lane == 0) okw = tc::mbar_wait(&mask_empty[u & 1], ((u >> 1) & 1) ^ 1, err, 12);
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) break;
+          const uint32_t bal0 = __ballot_sync(0xffffffffu, cur.s0.valid);
+          const uint32_t bal1 = __ballot_sync(0xffffffffu, has1 && cur.s1.valid);
+          if (lane == 0) {
+            smask[(u & 1) * 4 + warp] = bal0;
+            if (warp == 0) smask[(u & 1) * 4 + 3] = bal1;
+          }
+          if (kE4M3) {
+            svscale[(u & 1) * 128 + pt] =
+                (cur.s0.valid && !cur.s0.win) ? __ldg(a.kscale + cur.s0.row) : 1.f;
+            if (has1)
+              svscale[(u & 1) * 128 + pt + kProd] =
+                  (cur.s1.valid && !cur.s1.win) ? __ldg(a.kscale + cur.s1.row) : 1.f;
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
+          for (int cc = 0; cc < a.nsc && ok; ++cc)
+            ok = cc < a.nc ? issue_chunk(cc, kHi, cur.rr, cur.wb)
+                           : issue_chunk(cc - a.nc, kLo, cur.rr, cur.wb);
+          // the next tile's rows are looked up before the value chunks of the
+          // previous tile go out, so their arrivals (deferred to the next
+          // issues) do not wait on the index-list loads
+          if (u + 1 < n) tile_rows(u + 1, nxt);
+        }
+        if (u >= 1)
+          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev.rr, prev.wb);
+        prev = cur;
+        cur = nxt;
       }
-      if (u >= 1)
-        for (int c = 0; c < a.nvc && ok; ++c) ok = load_chunk(vc0 + c, kVal, prev);
-      prev = cur;
+      // every copy must land before the CTA can exit; arrive for the chunks
+      // still pending
+      cp_async_wait<0>();
+      if (!kE4M3) {
+        tc::fence_proxy_async_smem();
+        for (uint32_t j = lt - pend; j < lt; ++j) tc::mbar_arrive(&ring_full[j % kRing]);
+      }
+      if (pt == 0) tc::mbar_drain(q_full, 0);
     }
-    // let this CTA's copies in flight land before it can exit
-    if (!kE4M3 && lane == 0)
-      for (uint32_t j = lt > (uint32_t)kRing ? lt - kRing : 0; j < lt; ++j)
-        tc::mbar_drain(&ring_full[j % kRing], (j / kRing) & 1);
-    if (lane == 0) tc::mbar_drain(q_full, 0);
-  } else if (warp == 1 && n > 0) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && n > 0) {
       const uint32_t id_s = tc::idesc(128, kT, 1, 1);
       const uint32_t id_pv = tc::idesc(128, 64, 1, 1, 0, 1);
       uint32_t lt = 0;
@@ -419,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(mma_done);
       tc::mbar_drain(mma_done, 0);
     }
-  } else if (warp >= 2) {
-    // ------------------------------------------------------------ softmax
+  } else {
+    // ------------------------------------------------------------ softmax (warps 4-7)
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -454,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_tile = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kT; ++j) {
-        const bool v = (bal[j & 3] >> (j >> 2)) & 1u;
+        const bool v = (bal[j >> 5] >> (j & 31)) & 1u;
         x[j] = v ? x[j] * a.c_log2 : -INFINITY;
         m_tile = fmaxf(m_tile, x[j]);
       }
@@ -601,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 512);
   }
@@ -781,6 +825,7 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.q_pos0 = q_pos0;
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.idx = idx;
+  a.kv16 = reinterpret_cast<const uint16_t*>(kv.data);
   a.codes = reinterpret_cast<const uint8_t*>(kv.data);
   a.rope = reinterpret_cast<const uint16_t*>(kv.rope);
   a.kscale = kv.scale;
@@ -795,16 +840,8 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
                                   ((rows * p.D_v * sizeof(float) + 255) & ~(size_t)255));
 
-  CUtensorMap tm_q, tm_kv, tm_raw;
-  memset(&tm_kv, 0, sizeof(tm_kv));
-  memset(&tm_raw, 0, sizeof(tm_raw));
+  CUtensorMap tm_q;
   if (!make_map_bf16(&tm_q, q, (int64_t)p.B * Q * p.H, p.D_qk, 128)) return cudaErrorInvalidValue;
-  if (!a.e4m3) {
-    if (!make_map_bf16(&tm_kv, kv.data, (int64_t)p.B * kv.n_rows, p.D_qk, 1))
-      return cudaErrorInvalidValue;
-    if (p.window > 0 && !make_map_bf16(&tm_raw, raw.data, (int64_t)p.B * raw.n_rows, p.D_qk, 1))
-      return cudaErrorInvalidValue;
-  }
   const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
@@ -814,12 +851,12 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
+    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, a);
   } else {
     e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
+    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
