@@ -239,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* mask_full = p_full + 2;   // [2]
   uint64_t* mask_empty = mask_full + 2;  // [2]
-  uint64_t* o_done = mask_empty + 2;
-  uint64_t* mma_done = o_done + 1;
+  // PV(u) completes o_done[u & 1]: with two barriers no waiter can fall two
+  // phases behind (a parity wait cannot tell phase j from phase j + 2)
+  uint64_t* o_done = mask_empty + 2;  // [2]
+  uint64_t* mma_done = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   uint32_t* smask = tmem_slot + 4;  // [2][4] ballot words of the tile's valid slots
   float* svscale = reinterpret_cast<float*>(smask + 8);  // e4m3: [2][128] row scales of the tile
@@ -274,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&mask_full[s], kProdWarps);
       tc::mbar_init(&mask_empty[s], 4);
     }
-    tc::mbar_init(o_done, 1);
+    tc::mbar_init(&o_done[0], 1);
+    tc::mbar_init(&o_done[1], 1);
     tc::mbar_init(mma_done, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tm_q);
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_commit(&ring_empty[slot]);
           ++lt;
         }
-        tc::mma_commit(o_done);
+        tc::mma_commit(&o_done[u & 1]);
         return true;
       };
       for (int u = 0; u < n && ok; ++u) {
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = grow ? exp2f(m_ref - m_tile) : 1.f;
       if (__any_sync(0xffffffffu, rescale)) {
         // O holds the tiles before u: wait for PV(u-1), then scale the rows
-        okw = lane == 0 ? (int)tc::mbar_wait(o_done, (u - 1) & 1, err, 33) : 0;
+        okw = lane == 0 ? (int)tc::mbar_wait(&o_done[(u - 1) & 1], ((u - 1) >> 1) & 1, err, 33) : 0;
         okw = __shfl_sync(0xffffffffu, okw, 0);
         __syncwarp();
         if (!okw) { ok = false; break; }
@@ -567,13 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     bool have_o = ok && n > 0;
     if (have_o) {
-      // PV(n-3) has completed (it precedes S(n-1)), so o_done has finished at
-      // least n-2 phases: wait for phase n-2, then n-1, one parity at a time
+      // PV(n-1) is the ((n-1)/2)-th completion of o_done[(n-1) & 1]; that
+      // barrier cannot be further ahead (no PV(n+1))
       int okw = 1;
-      if (lane == 0) {
-        if (n >= 2) okw = tc::mbar_wait(o_done, (n - 2) & 1, err, 34);
-        if (okw) okw = tc::mbar_wait(o_done, (n - 1) & 1, err, 35);
-      }
+      if (lane == 0) okw = tc::mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, err, 35);
       okw = __shfl_sync(0xffffffffu, okw, 0);
       __syncwarp();
       have_o = okw != 0;
@@ -845,7 +845,7 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
-                      (2 * kRing + 12) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
+                      (2 * kRing + 13) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
   cudaError_t e;
   if (a.e4m3) {
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -46,8 +46,9 @@ struct Vec<T, 1> {
   }
 };
 
-// float64 recompute of one channel; used when the fp32 result lies too close
-// to a bfloat16 rounding boundary to decide the rounding.
+// float64 recompute of one channel: the last resort for a result that even
+// the double-float evaluation below cannot place on one side of a bfloat16
+// rounding boundary (float64 is slow on this part, so it must stay rare).
 template <typename T>
 __device__ double pool_f64(const void* x, const void* g, const float* bias, int64_t row0, int C,
                            int m, int c) {
@@ -69,8 +70,143 @@ __device__ double pool_f64(const void* x, const void* g, const float* bias, int6
   return A / S;
 }
 
+// ---- double-float arithmetic: a value is the unevaluated sum hi + lo of two
+// floats (about 48 significant bits), built on the error-free transformations
+// TwoSum (Knuth) and TwoProduct (Dekker, here with a fused multiply-add).
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff ff_two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ ff ff_fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = ff_two_sum(a.hi, b.hi);
+  const ff t = ff_two_sum(a.lo, b.lo);
+  s.lo += t.hi;
+  s = ff_fast_two_sum(s.hi, s.lo);
+  s.lo += t.lo;
+  return ff_fast_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+  const float p = a.hi * b;
+  float e = fmaf(a.hi, b, -p);
+  e = fmaf(a.lo, b, e);
+  return ff_fast_two_sum(p, e);
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return ff_fast_two_sum(p, e);
+}
+// a / b by two Newton corrections of the float quotient.
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  const float q1 = a.hi / b.hi;
+  ff r = ff_add(a, ff_mul_f(b, -q1));
+  const float q2 = r.hi / b.hi;
+  r = ff_add(r, ff_mul_f(b, -q2));
+  const float q3 = r.hi / b.hi;
+  return ff_add(ff_fast_two_sum(q1, q2), ff{q3, 0.f});
+}
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
+// 1/n! for n = 0..13 as double-floats (high part: the float nearest 1/n!;
+// low part: the float nearest the rest).
+__constant__ float c_inv_fact[14][2] = {
+    {1.0f, 0.0f},
+    {1.0f, 0.0f},
+    {0.5f, 0.0f},
+    {0.1666666716337204f, -4.967053879312289e-09f},
+    {0.0416666679084301f, -1.2417634698280722e-09f},
+    {0.008333333767950535f, -4.34617203337595e-10f},
+    {0.0013888889225199819f, -3.3631094437103215e-11f},
+    {0.00019841270113829523f, -2.725596874933456e-12f},
+    {2.4801587642286904e-05f, -3.40699609366682e-13f},
+    {2.7557318844628753e-06f, 3.793571224297229e-14f},
+    {2.755731998149713e-07f, -7.575112209051195e-15f},
+    {2.5052107943679403e-08f, 4.4176230446483665e-16f},
+    {2.0876755879584152e-09f, 1.1082839147459852e-16f},
+    {1.6059044372074283e-10f, -5.352526511562726e-18f},
+};
+
+// e^d for d <= 0 in double-float: Cody-Waite reduction d = k ln2 + r
+// (|r| <= ln2/2, ln2 held as a double-float) and the Taylor series of e^r to
+// degree 13 (|r|^14/14! < 2^-50), evaluated in Horner form.
+__device__ ff ff_exp_nonpos(ff d) {
+  if (d.hi < -120.f) return ff{0.f, 0.f};  // below 2^-173: nothing next to the e^0 term
+  const float ln2_hi = 0.693147182464599609375f;        // float nearest to ln 2
+  const float ln2_lo = -1.904654323148236017e-09f;      // ln 2 - ln2_hi
+  const float k = rintf(d.hi * 1.44269504088896340736f);
+  // k * ln2 as a double-float: k * ln2_hi exactly (TwoProduct), plus k * ln2_lo
+  const float p = k * ln2_hi;
+  const ff kl = ff_fast_two_sum(p, fmaf(k, ln2_hi, -p) + k * ln2_lo);
+  const ff r = ff_add(d, ff{-kl.hi, -kl.lo});
+  ff s{c_inv_fact[13][0], c_inv_fact[13][1]};
+#pragma unroll
+  for (int n = 12; n >= 0; --n) s = ff_add(ff_mul(s, r), ff{c_inv_fact[n][0], c_inv_fact[n][1]});
+  const int ki = (int)k;
+  return ff{ldexpf(s.hi, ki), ldexpf(s.lo, ki)};
+}
+
+// Pooled value of one channel in double-float; *mag (if given) receives
+// sum_i w_i |x_i|, the scale its error is relative to (about 2^-44 of it).
+template <typename T>
+__device__ ff pool_ff(const void* x, const void* g, const float* bias, int64_t row0, int C, int m,
+                      int c, float* mag = nullptr) {
+  ff mx{-INFINITY, 0.f};
+  for (int i = 0; i < m; ++i) {
+    float gv;
+    Vec<T, 1>::load(g, (row0 + i) * C + c, &gv);
+    const ff z = ff_two_sum(gv, bias[i * C + c]);  // exact
+    if (i == 0 || ff_gt(z, mx)) mx = z;
+  }
+  ff S{0.f, 0.f}, A{0.f, 0.f};
+  for (int i = 0; i < m; ++i) {
+    float gv, xv;
+    Vec<T, 1>::load(g, (row0 + i) * C + c, &gv);
+    Vec<T, 1>::load(x, (row0 + i) * C + c, &xv);
+    const ff z = ff_two_sum(gv, bias[i * C + c]);
+    const ff e = ff_exp_nonpos(ff_add(z, ff{-mx.hi, -mx.lo}));
+    S = ff_add(S, e);
+    A = ff_add(A, ff_mul_f(e, xv));
+    if (mag) *mag += e.hi * fabsf(xv);
+  }
+  if (mag) *mag /= S.hi;
+  return ff_div(A, S);
+}
+
+// The bfloat16 nearest to the exact pooled value.  hi + lo is within about
+// 2^-44 * sum w|x| of it.  Unless the sum cancels by more than 2^14 (then
+// float64 decides), that is far below half a float ulp of hi, so hi + lo
+// rounds the same way as the exact value unless hi is itself a rounding
+// midpoint (every other float is a full float ulp away from the nearest
+// midpoint); then the sign of lo decides, and a lo too small to trust sends
+// the channel to float64.
+template <typename T>
+__device__ uint16_t pool_bf16_exact(const void* x, const void* g, const float* bias, int64_t row0,
+                                    int C, int m, int c) {
+  float mag = 0.f;
+  const ff v = pool_ff<T>(x, g, bias, row0, C, m, c, &mag);
+  const uint32_t hb = __float_as_uint(v.hi);
+  const bool cancels = mag > ldexpf(fabsf(v.hi), 14);
+  const bool midpoint = (hb & 0xffffu) == 0x8000u;
+  if (cancels || (midpoint && fabsf(v.lo) <= ldexpf(fabsf(v.hi), -28)))
+    return __bfloat16_as_ushort(__double2bfloat16(pool_f64<T>(x, g, bias, row0, C, m, c)));
+  if (!midpoint) return __bfloat16_as_ushort(__float2bfloat16_rn(v.hi));
+  const uint16_t t = (uint16_t)(hb >> 16);  // truncated: the midpoint's smaller magnitude side
+  return ((v.lo > 0.f) == (v.hi > 0.f)) ? (uint16_t)(t + 1) : t;
+}
+
 // out_mode: 0 = fp32 rows, 1 = bf16 rounded from the fp32 result,
-//           2 = bf16 nearest to the exact result (guard band + fp64 recompute).
+//           2 = bf16 nearest to the exact result (guard band + double-float
+//               recompute of the channels too close to a rounding boundary).
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ x,
                                                        const void* __restrict__ g,
@@ -142,7 +278,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ 
           __nv_bfloat16 lo = __float2bfloat16_rn(r - guard);
           __nv_bfloat16 hi = __float2bfloat16_rn(r + guard);
           if (__bfloat16_as_ushort(lo) != __bfloat16_as_ushort(hi))
-            h = __double2bfloat16(pool_f64<T>(x, g, bias, row0, C, m, c0 + v));
+            h = __ushort_as_bfloat16(pool_bf16_exact<T>(x, g, bias, row0, C, m, c0 + v));
         }
         o[v] = __bfloat16_as_ushort(h);
       }
@@ -150,7 +286,8 @@ __global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ 
   }
 }
 
-// Mixed e4m3 + bf16 output: one block per entry, float64 arithmetic.
+// Mixed e4m3 + bf16 output: one block per entry; the pooled values in
+// double-float (exact in float64), then the row scale and the codes in float64.
 template <typename T>
 __global__ void __launch_bounds__(256) compress_e4m3_kernel(
     const void* __restrict__ x, const void* __restrict__ g, const float* __restrict__ bias,
@@ -164,7 +301,8 @@ __global__ void __launch_bounds__(256) compress_e4m3_kernel(
   const int64_t row0 = (int64_t)b * T_rows + s * m - row_off;
   double amax = 0.0;
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    double v = pool_f64<T>(x, g, bias, row0, C, m, c);
+    const ff pv = pool_ff<T>(x, g, bias, row0, C, m, c);
+    const double v = (double)pv.hi + (double)pv.lo;
     vals[c] = v;
     if (c < nope) amax = fmax(amax, fabs(v));
   }
@@ -221,8 +359,12 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
     int64_t cap = (int64_t)sms * 16;
     return (unsigned)(blocks < cap ? blocks : cap);
   };
+  // Few entries (a decode step): one channel per thread.  The rare channels
+  // that need the exact-rounding recompute then sit in different threads (a
+  // warp runs its lanes' recomputes one after another), and the grid is wider.
+  const bool few = (int64_t)B * n_s * m < 4096;
   if (in_dtype == CSA_F32) {
-    if (C % 4 == 0)
+    if (C % 4 == 0 && !few)
       compress_kernel<float, 4><<<grid_for(4), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m, C,
                                                              s_begin, n_s, out.data, out.n_rows,
                                                              out_mode);
@@ -231,7 +373,7 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
                                                              s_begin, n_s, out.data, out.n_rows,
                                                              out_mode);
   } else {
-    if (C % 8 == 0)
+    if (C % 8 == 0 && !few)
       compress_kernel<uint16_t, 8><<<grid_for(8), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m,
                                                                 C, s_begin, n_s, out.data,
                                                                 out.n_rows, out_mode);

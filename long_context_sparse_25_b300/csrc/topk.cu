@@ -150,30 +150,36 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float* __restr
 
 
 // ------------------------------------------------------------------------
-// Long rows with few rows (decode: B rows of 10^5..10^6 entries) are split
-// over many CTAs in three kernels:
-//   A  hist:   each CTA histograms the top kDigitBits bits of its slice's keys
-//              into the row's global histogram;
-//   B  filter: each CTA finds the boundary digit (the one holding the kk-th
-//              largest key), appends every index with a larger digit to the
-//              row's "selected" list and every (key, index) with the boundary
-//              digit to the row's candidate list;
-//   C  final:  one CTA per row picks the still-needed candidates exactly, by
-//              a radix select on the 64-bit composite (key << 32 | ~index),
-//              whose values are all distinct and order ties by lower index;
-//              then sorts the kk indices ascending (bitonic, shared memory).
-// The lists are filled in whatever order the atomics give, but the final
-// set is unique and sorted, so the output is deterministic.
-constexpr int kDigitBits = 12;
-constexpr int kBins = 1 << kDigitBits;
-constexpr int kMaxK = 4096;         // bitonic sort capacity of kernel C
-constexpr int kCandSmem = 3840;     // candidates kept in shared memory by kernel C (static smem < 48 KB)
+// Long rows with few rows (decode: B rows of 10^5..10^6 entries), in three
+// kernels over the order-preserving 32-bit keys:
+//   A  sample: one CTA per row radix-selects, from 4096 evenly spaced keys of
+//              the row, the key tau of rank r = 4 k ns / n: about 4k keys of
+//              the row are >= tau;
+//   B  filter: S CTAs per row; each warp compacts its contiguous part of the
+//              row, in index order (ballots), into a list of the (key, index)
+//              composites of its keys >= tau;
+//   C  final:  one CTA per row; if at least kk keys reached tau the kk largest
+//              of the row are all among them: an exact radix select on the
+//              64-bit composite (key << 32 | ~index), whose values are all
+//              distinct and order ties by lower index, gives the threshold, and
+//              the composites at or above it, already in index order, are the
+//              output.  If fewer reached tau (a sample far from the row, never
+//              seen on these workloads), the CTA selects over the whole row.
+// A histogram of the raw key bits would do the same in one pass, but scores
+// often share a few binades, so its atomics pile up on a handful of bins.
+constexpr int kMaxK = 4096;         // largest k of this path
+constexpr int kSample = 4096;       // keys sampled per row
+constexpr int kCandSmem = 8192;     // candidates kernel C keeps in shared memory
+constexpr int kWarpsB = 16;         // warps of kernel B (512 threads)
+constexpr int kMaxSlices = 256;     // slices x kWarpsB lists fit kernel C's shared memory
+constexpr int kMaxLists = kMaxSlices * kWarpsB;
+constexpr int kTargetCtas = 592;    // slices of all rows together (4 x 148), device independent
 
 struct LongRows {
-  int* hist;          // [rows][kBins]
-  int* counts;        // [rows][2]: selected, candidates
-  int32_t* selected;  // [rows][k]
-  unsigned long long* cand;  // [rows][N]
+  int S;                     // slices per row
+  uint32_t* tau;             // [rows]
+  int* cnt;                  // [rows][S * kWarpsB]
+  unsigned long long* cand;  // [rows][N]: each warp's candidates from its part's start
 };
 
 __device__ __forceinline__ int64_t row_visible(int64_t row, int Q, int64_t q_pos0, int m, int64_t N) {
@@ -182,114 +188,22 @@ __device__ __forceinline__ int64_t row_visible(int64_t row, int Q, int64_t q_pos
   return nv < N ? nv : N;
 }
 
-__global__ void __launch_bounds__(512) topk_hist_kernel(const float* __restrict__ scores,
-                                                        int64_t q_pos0, int Q, int64_t N, int m,
-                                                        int k, LongRows lr) {
-  __shared__ int h[kBins];
-  const int64_t row = blockIdx.y;
-  const int64_t n = row_visible(row, Q, q_pos0, m, N);
-  if (n <= k) return;  // everything kept: kernel C handles it directly
-  for (int j = threadIdx.x; j < kBins; j += blockDim.x) h[j] = 0;
-  __syncthreads();
-  const int64_t per = (n + gridDim.x - 1) / gridDim.x;
-  const int64_t s0 = blockIdx.x * per, s1 = s0 + per < n ? s0 + per : n;
-  const float* srow = scores + row * N;
-  for (int64_t s = s0 + threadIdx.x; s < s1; s += blockDim.x)
-    atomicAdd(&h[score_key(__ldg(srow + s)) >> (32 - kDigitBits)], 1);
-  __syncthreads();
-  int* gh = lr.hist + row * kBins;
-  for (int j = threadIdx.x; j < kBins; j += blockDim.x)
-    if (h[j]) atomicAdd(&gh[j], h[j]);
+// part `part` of `parts` equal parts of [0, n)
+__device__ __forceinline__ void part_range(int64_t n, int parts, int part, int64_t* p0, int64_t* p1) {
+  *p0 = n * part / parts;
+  *p1 = n * (part + 1) / parts;
 }
 
-// boundary digit of a row from its histogram (block-wide), with the count of
-// keys in larger digits
-__device__ void find_boundary(const int* gh, int kk, int* sh, int* out_digit, int* out_above) {
-  // sh: kBins ints of shared memory; suffix sums from the top digit down
-  for (int j = threadIdx.x; j < kBins; j += blockDim.x) sh[j] = gh[j];
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int above = 0;
-    for (int base = kBins - 32; base >= 0; base -= 32) {
-      const int d = base + 31 - lane;  // lane 0: largest digit of the chunk
-      const int c = sh[d];
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      unsigned hit = __ballot_sync(0xffffffffu, above + incl >= kk);
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        const int excl = __shfl_sync(0xffffffffu, incl - c, l);
-        if (lane == 0) {
-          *out_digit = base + 31 - l;
-          *out_above = above + excl;
-        }
-        break;
-      }
-      above += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  __syncthreads();
-}
-
-__global__ void __launch_bounds__(512) topk_filter_kernel(const float* __restrict__ scores,
-                                                          int64_t q_pos0, int Q, int64_t N, int m,
-                                                          int k, LongRows lr) {
-  __shared__ int sh[kBins];
-  __shared__ int digit, above;
-  const int64_t row = blockIdx.y;
-  const int64_t n = row_visible(row, Q, q_pos0, m, N);
-  if (n <= k) return;
-  find_boundary(lr.hist + row * kBins, k, sh, &digit, &above);
-  const uint32_t dstar = (uint32_t)digit;
-  const int64_t per = (n + gridDim.x - 1) / gridDim.x;
-  const int64_t s0 = blockIdx.x * per, s1 = s0 + per < n ? s0 + per : n;
-  const float* srow = scores + row * N;
-  int* cnt = lr.counts + row * 2;
-  int32_t* sel = lr.selected + row * (int64_t)k;
-  unsigned long long* cand = lr.cand + row * N;
-  const int lane = threadIdx.x & 31;
-  for (int64_t base = s0; base < s1; base += blockDim.x) {
-    const int64_t s = base + threadIdx.x;
-    uint32_t key = 0, d = 0;
-    if (s < s1) {
-      key = score_key(__ldg(srow + s));
-      d = key >> (32 - kDigitBits);
-    }
-    const bool up = s < s1 && d > dstar;
-    const bool eq = s < s1 && d == dstar;
-    unsigned mu = __ballot_sync(0xffffffffu, up);
-    unsigned me = __ballot_sync(0xffffffffu, eq);
-    int bu = 0, be = 0;
-    if (lane == 0) {
-      if (mu) bu = atomicAdd(&cnt[0], __popc(mu));
-      if (me) be = atomicAdd(&cnt[1], __popc(me));
-    }
-    bu = __shfl_sync(0xffffffffu, bu, 0);
-    be = __shfl_sync(0xffffffffu, be, 0);
-    const unsigned lower = (1u << lane) - 1u;
-    if (up) sel[bu + __popc(mu & lower)] = (int32_t)s;
-    if (eq)
-      cand[be + __popc(me & lower)] =
-          ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)s);
-  }
-}
-
-// radix select over 64-bit composites: the `need`-th largest (all distinct)
-template <bool kSmem>
-__device__ unsigned long long select_composite(const unsigned long long* v, int64_t n, int need,
-                                               int* hist, unsigned long long* sh_prefix,
-                                               int* sh_need) {
-  unsigned long long prefix = 0, mask = 0;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+// The need-th largest of get(i), i < n, by 8-bit radix passes from the top
+// (block-wide; values with bits above `bits` ignored).  Key type U.
+template <typename U, int kBits, typename Get>
+__device__ U radix_select(Get get, int64_t n, int need, int* hist, U* sh_prefix, int* sh_need) {
+  U prefix = 0, mask = 0;
+  for (int shift = kBits - 8; shift >= 0; shift -= 8) {
     for (int j = threadIdx.x; j < 256; j += blockDim.x) hist[j] = 0;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-      unsigned long long x = v[i];
+      const U x = get(i);
       if ((x & mask) == prefix) atomicAdd(&hist[(int)((x >> shift) & 255)], 1);
     }
     __syncthreads();
@@ -305,12 +219,12 @@ __device__ unsigned long long select_composite(const unsigned long long* v, int6
           int y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        unsigned hit = __ballot_sync(0xffffffffu, acc_above + incl >= need);
+        const unsigned hit = __ballot_sync(0xffffffffu, acc_above + incl >= need);
         if (hit) {
           const int l = __ffs(hit) - 1;
           const int excl = __shfl_sync(0xffffffffu, incl - c, l);
           if (lane == 0) {
-            *sh_prefix = prefix | ((unsigned long long)(chunk * 32 + 31 - l) << shift);
+            *sh_prefix = prefix | ((U)(chunk * 32 + 31 - l) << shift);
             *sh_need = need - (acc_above + excl);
           }
           break;
@@ -321,21 +235,117 @@ __device__ unsigned long long select_composite(const unsigned long long* v, int6
     __syncthreads();
     prefix = *sh_prefix;
     need = *sh_need;
-    mask |= 255ull << shift;
+    mask |= (U)255 << shift;
     __syncthreads();
   }
   return prefix;
 }
 
-__global__ void __launch_bounds__(1024) topk_final_kernel(int64_t q_pos0, int Q, int64_t N, int m,
+__global__ void __launch_bounds__(1024) topk_sample_kernel(const float* __restrict__ scores,
+                                                           int64_t q_pos0, int Q, int64_t N, int m,
+                                                           int k, LongRows lr) {
+  __shared__ uint32_t keys[kSample];
+  __shared__ int hist[256];
+  __shared__ uint32_t sh_prefix;
+  __shared__ int sh_need;
+  const int64_t row = blockIdx.x;
+  const int64_t n = row_visible(row, Q, q_pos0, m, N);
+  if (n <= k) return;
+  const int ns = n < kSample ? (int)n : kSample;
+  const float* srow = scores + row * N;
+  for (int j = threadIdx.x; j < ns; j += blockDim.x)
+    keys[j] = score_key(__ldg(srow + (int64_t)j * n / ns));
+  __syncthreads();
+  int64_t r = (4 * (int64_t)k * ns + n - 1) / n;
+  if (r > ns) r = ns;
+  if (r < 1) r = 1;
+  const uint32_t tau = radix_select<uint32_t, 32>([&](int64_t i) { return keys[i]; }, ns, (int)r,
+                                                  hist, &sh_prefix, &sh_need);
+  if (threadIdx.x == 0) lr.tau[row] = tau;
+}
+
+__global__ void __launch_bounds__(512) topk_filter_kernel(const float* __restrict__ scores,
+                                                          int64_t q_pos0, int Q, int64_t N, int m,
+                                                          int k, LongRows lr) {
+  const int64_t row = blockIdx.y;
+  const int s = blockIdx.x;
+  const int64_t n = row_visible(row, Q, q_pos0, m, N);
+  if (n <= k) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t tau = __ldcg(lr.tau + row);
+  int64_t s0, s1, w0, w1;
+  part_range(n, lr.S, s, &s0, &s1);
+  part_range(s1 - s0, kWarpsB, warp, &w0, &w1);
+  w0 += s0;
+  w1 += s0;
+  const float* srow = scores + row * N;
+  unsigned long long* cand = lr.cand + row * N + w0;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int nc = 0;
+  for (int64_t base = w0; base < w1; base += 8 * 32) {
+    uint32_t key[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t t = base + j * 32 + lane;
+      key[j] = t < w1 ? score_key(__ldg(srow + t)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t t = base + j * 32 + lane;
+      const unsigned b = __ballot_sync(0xffffffffu, t < w1 && key[j] >= tau);
+      if ((b >> lane) & 1u)
+        cand[nc + __popc(b & lt_mask)] =
+            ((unsigned long long)key[j] << 32) | (unsigned long long)(~(uint32_t)t);
+      nc += __popc(b);
+    }
+  }
+  if (lane == 0) lr.cnt[row * lr.S * kWarpsB + s * kWarpsB + warp] = nc;
+}
+
+// List holding flat position f of lists that start at off[0..L) (ascending).
+__device__ __forceinline__ int find_list(const int* off, int L, int f) {
+  int lo = 0, hi = L - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= f) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Exclusive prefix of cnt[0..L) into off[0..L) (shared), L <= kMaxLists, by a
+// 1024-thread block; returns the total.
+__device__ int list_offsets(const int* cnt, int L, int* off, int* warp_sums) {
+  constexpr int kPer = kMaxLists / 1024;
+  const int l0 = threadIdx.x * kPer;
+  int v[kPer], local = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    v[j] = l0 + j < L ? __ldcg(cnt + l0 + j) : 0;
+    local += v[j];
+  }
+  int total;
+  int acc = BlockScan::run(local, warp_sums, &total);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    if (l0 + j < L) off[l0 + j] = acc;
+    acc += v[j];
+  }
+  return total;
+}
+
+__global__ void __launch_bounds__(1024) topk_final_kernel(const float* __restrict__ scores,
+                                                          int64_t q_pos0, int Q, int64_t N, int m,
                                                           int k, LongRows lr,
                                                           int32_t* __restrict__ idx) {
+  extern __shared__ unsigned long long dsm[];
+  unsigned long long* cbuf = dsm;                          // [kCandSmem]
+  int* off = reinterpret_cast<int*>(cbuf + kCandSmem);     // [kMaxLists]
   __shared__ int hist[256];
-  __shared__ unsigned long long sh_prefix;
-  __shared__ int sh_need;
-  __shared__ int sort_buf[kMaxK];
-  __shared__ unsigned long long cbuf[kCandSmem];
-  __shared__ int sh_taken;
+  __shared__ int warp_sums[32];
+  __shared__ unsigned long long sh_prefix64;
+  __shared__ uint32_t sh_prefix32;
+  __shared__ int sh_need, sh_nc;
   const int64_t row = blockIdx.x;
   const int64_t n = row_visible(row, Q, q_pos0, m, N);
   int32_t* orow = idx + row * (int64_t)k;
@@ -345,52 +355,70 @@ __global__ void __launch_bounds__(1024) topk_final_kernel(int64_t q_pos0, int Q,
     for (int j = threadIdx.x; j < kk; j += blockDim.x) orow[j] = j;
     return;
   }
-  const int n_up = lr.counts[row * 2 + 0];
-  const int n_cand = lr.counts[row * 2 + 1];
-  const int need = kk - n_up;  // >= 1 by construction of the boundary digit
-  const unsigned long long* cand = lr.cand + row * N;
+  const int S = lr.S, L = S * kWarpsB;
+  {
+    const int c = list_offsets(lr.cnt + row * L, L, off, warp_sums);
+    if (threadIdx.x == 0) sh_nc = c;
+  }
+  __syncthreads();
+  const int nc = sh_nc;
+  const float* srow = scores + row * N;
+  if (nc < kk) {
+    // fewer than kk keys reached tau: exact select over the whole row (the
+    // kk-th largest key, then every larger key and the lowest-index equal
+    // ones, in index order)
+    const uint32_t T = radix_select<uint32_t, 32>(
+        [&](int64_t i) { return score_key(__ldg(srow + i)); }, n, kk, hist, &sh_prefix32, &sh_need);
+    const int need_eq = sh_need;  // keys equal to T still needed
+    int taken = 0, eq_seen = 0;
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+      const int64_t t = base + threadIdx.x;
+      const uint32_t kx = t < n ? score_key(__ldg(srow + t)) : 0u;
+      const int gt = (t < n && kx > T) ? 1 : 0;
+      const int eq = (t < n && kx == T) ? 1 : 0;
+      int eq_tot, take_tot;
+      const int eq_rank = eq_seen + BlockScan::run(eq, warp_sums, &eq_tot);
+      const int take = gt | (eq & (eq_rank < need_eq ? 1 : 0));
+      const int pos = taken + BlockScan::run(take, warp_sums, &take_tot);
+      if (take) orow[pos] = (int32_t)t;
+      taken += take_tot;
+      eq_seen += eq_tot;
+    }
+    return;
+  }
+  // list l covers [list_start(l), ...) of the row: slice l / kWarpsB, warp part l % kWarpsB
+  auto list_start = [&](int l) -> int64_t {
+    int64_t s0, s1, w0, w1;
+    part_range(n, S, l / kWarpsB, &s0, &s1);
+    part_range(s1 - s0, kWarpsB, l % kWarpsB, &w0, &w1);
+    return s0 + w0;
+  };
+  auto cand_at = [&](int64_t f) -> unsigned long long {
+    const int l = find_list(off, L, (int)f);
+    return __ldcg(lr.cand + row * N + list_start(l) + (f - off[l]));
+  };
+  const bool in_smem = nc <= kCandSmem;
+  if (in_smem)
+    for (int f = threadIdx.x; f < nc; f += blockDim.x) cbuf[f] = cand_at(f);
+  __syncthreads();
   unsigned long long thr;
-  const bool in_smem = n_cand <= kCandSmem;
-  if (in_smem) {
-    for (int j = threadIdx.x; j < n_cand; j += blockDim.x) cbuf[j] = cand[j];
-    __syncthreads();
-    thr = select_composite<true>(cbuf, n_cand, need, hist, &sh_prefix, &sh_need);
-  } else {
-    thr = select_composite<false>(cand, n_cand, need, hist, &sh_prefix, &sh_need);
+  if (in_smem)
+    thr = radix_select<unsigned long long, 64>([&](int64_t i) { return cbuf[i]; }, nc, kk, hist,
+                                               &sh_prefix64, &sh_need);
+  else
+    thr = radix_select<unsigned long long, 64>(cand_at, nc, kk, hist, &sh_prefix64, &sh_need);
+  // the composites at or above thr are the kk kept entries, already in index order
+  int taken = 0;
+  for (int base = 0; base < nc; base += blockDim.x) {
+    const int f = base + threadIdx.x;
+    unsigned long long x = 0;
+    if (f < nc) x = in_smem ? cbuf[f] : cand_at(f);
+    const bool take = f < nc && x >= thr;
+    int tot;
+    const int pre = BlockScan::run(take ? 1 : 0, warp_sums, &tot);
+    if (take) orow[taken + pre] = (int32_t)(~(uint32_t)(x & 0xffffffffull));
+    taken += tot;
   }
-  // gather the kk indices
-  const int32_t* sel = lr.selected + row * (int64_t)k;
-  for (int j = threadIdx.x; j < n_up; j += blockDim.x) sort_buf[j] = sel[j];
-  if (threadIdx.x == 0) sh_taken = n_up;
-  __syncthreads();
-  for (int j = threadIdx.x; j < n_cand; j += blockDim.x) {
-    const unsigned long long x = in_smem ? cbuf[j] : cand[j];
-    if (x >= thr) {
-      const int pos = atomicAdd(&sh_taken, 1);
-      sort_buf[pos] = (int)(~(uint32_t)(x & 0xffffffffull));
-    }
-  }
-  __syncthreads();
-  int P = 1;
-  while (P < kk) P <<= 1;
-  for (int j = kk + threadIdx.x; j < P; j += blockDim.x) sort_buf[j] = 0x7fffffff;
-  __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < P / 2; t += blockDim.x) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const bool asc = (i & size) == 0;
-        const int a = sort_buf[i], b = sort_buf[j];
-        if ((a > b) == asc) {
-          sort_buf[i] = b;
-          sort_buf[j] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int j = threadIdx.x; j < kk; j += blockDim.x) orow[j] = sort_buf[j];
 }
 
 bool use_long_rows(const csa_params& p, int Q, int64_t N) {
@@ -398,18 +426,28 @@ bool use_long_rows(const csa_params& p, int Q, int64_t N) {
   return N > kSmemRow && p.k <= kMaxK && rows < 256;
 }
 
+int long_rows_slices(const csa_params& p, int Q, int64_t N) {
+  const int64_t rows = (int64_t)p.B * Q;
+  int64_t S = ceil_div(kTargetCtas, rows);
+  const int64_t cap = ceil_div(N, 2048);
+  if (S > cap) S = cap;
+  if (S > kMaxSlices) S = kMaxSlices;
+  return S < 1 ? 1 : (int)S;
+}
+
+// Workspace layout; off[0..2] receive the offsets of the fields of LongRows.
 size_t long_rows_bytes(const csa_params& p, int Q, int64_t N, size_t* off) {
   const int64_t rows = (int64_t)p.B * Q;
+  const int S = long_rows_slices(p, Q, N);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t r = o;
     o += (bytes + 255) & ~(size_t)255;
     return r;
   };
-  off[0] = take((size_t)rows * kBins * sizeof(int));
-  off[1] = take((size_t)rows * 2 * sizeof(int));
-  off[2] = take((size_t)rows * p.k * sizeof(int32_t));
-  off[3] = take((size_t)rows * N * sizeof(unsigned long long));
+  off[0] = take((size_t)rows * sizeof(uint32_t));                 // tau
+  off[1] = take((size_t)rows * S * kWarpsB * sizeof(int));        // cnt
+  off[2] = take((size_t)rows * N * sizeof(unsigned long long));   // cand
   return o;
 }
 
@@ -417,7 +455,7 @@ size_t long_rows_bytes(const csa_params& p, int Q, int64_t N, size_t* off) {
 
 size_t topk_workspace(const csa_params& p, int Q, int64_t N) {
   if (!use_long_rows(p, Q, N)) return 0;
-  size_t off[4];
+  size_t off[3];
   return long_rows_bytes(p, Q, N, off);
 }
 
@@ -428,26 +466,22 @@ cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0
   const int64_t rows = (int64_t)p.B * Q;
   if (rows <= 0) return cudaSuccess;
   if (use_long_rows(p, Q, N)) {
-    size_t off[4];
-    const size_t bytes = long_rows_bytes(p, Q, N, off);
+    size_t off[3];
+    long_rows_bytes(p, Q, N, off);
     char* w = reinterpret_cast<char*>(ws);
-    LongRows lr{reinterpret_cast<int*>(w + off[0]), reinterpret_cast<int*>(w + off[1]),
-                reinterpret_cast<int32_t*>(w + off[2]),
-                reinterpret_cast<unsigned long long*>(w + off[3])};
-    (void)bytes;
-    cudaError_t e = cudaMemsetAsync(w, 0, off[2], st);  // histograms and counters
+    LongRows lr;
+    lr.S = long_rows_slices(p, Q, N);
+    lr.tau = reinterpret_cast<uint32_t*>(w + off[0]);
+    lr.cnt = reinterpret_cast<int*>(w + off[1]);
+    lr.cand = reinterpret_cast<unsigned long long*>(w + off[2]);
+    topk_sample_kernel<<<(unsigned)rows, 1024, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
+    dim3 g((unsigned)lr.S, (unsigned)rows);
+    topk_filter_kernel<<<g, 32 * kWarpsB, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
+    const size_t smem = kCandSmem * sizeof(unsigned long long) + kMaxLists * sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(topk_final_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int slices = (int)ceil_div(4 * sms, rows);
-    const int64_t max_slices = ceil_div(N, 2048);
-    if (slices > max_slices) slices = (int)max_slices;
-    if (slices < 1) slices = 1;
-    dim3 g((unsigned)slices, (unsigned)rows);
-    topk_hist_kernel<<<g, 512, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
-    topk_filter_kernel<<<g, 512, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
-    topk_final_kernel<<<(unsigned)rows, 1024, 0, st>>>(q_pos0, Q, N, p.m, p.k, lr, idx);
+    topk_final_kernel<<<(unsigned)rows, 1024, smem, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr, idx);
     return cudaGetLastError();
   }
   if (N <= kSmemRow) {

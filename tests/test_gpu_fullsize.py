@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle as O
-from long_context_sparse_25_b300 import synth
+from long_context_sparse_25_b300 import csa, synth
 from long_context_sparse_25_b300.pipeline import Step
 
 from harness import check_out, check_scores, check_selection, f64
@@ -23,6 +23,7 @@ def _decode_parity(wl, dev, attn_seqs):
     step = Step(wl, inp)
     step.run()
     torch.cuda.synchronize()
+    csa.device_status()  # no bounded device-side wait gave up
     N, m = wl.N, wl.m
     pos = np.array([wl.q_pos0])
     sel_all = step.selected().cpu().numpy()
@@ -86,6 +87,7 @@ def test_prefill_64k_full_size(cuda_device):
     step = Step(wl, inp)
     step.run()
     torch.cuda.synchronize()
+    csa.device_status()  # no bounded device-side wait gave up
     m, N = wl.m, wl.N
     qs = np.unique(np.concatenate([np.arange(128), np.arange(0, wl.Q, 256),
                                    np.arange(wl.Q - 128, wl.Q)]))

@@ -45,6 +45,7 @@ def _run(wl, dev):
     step = Step(wl, inp)
     step.run()
     torch.cuda.synchronize()
+    csa.device_status()  # no bounded device-side wait gave up
     return inp, step
 
 
@@ -133,6 +134,25 @@ def test_topk_bit_exact_on_oracle_scores(cuda_device):
         for b in range(B):
             ref = O.topk(s32[b].astype(np.float64), pos, m, k)
             assert np.array_equal(got[b], ref)
+
+
+def test_topk_long_row_whose_sample_misleads(cuda_device):
+    """A long row whose largest scores sit exactly at the evenly spaced
+    positions the multi-CTA path samples (4096 of n): too few keys reach the
+    sampled threshold, and the path must fall back to an exact select over
+    the whole row.  Output must equal the oracle's index list."""
+    rng = np.random.default_rng(9)
+    N, k, m = 20000, 1024, 4
+    q_pos0 = m * N - 1
+    s = rng.standard_normal((1, 1, N)).astype(np.float32)
+    ns = 4096
+    pos = (np.arange(ns, dtype=np.int64) * N) // ns
+    s[0, 0, pos] = 100.0 + np.arange(ns, dtype=np.float32) * 1e-3
+    p = csa.params(1, m, k=k)
+    idx = torch.empty((1, 1, k), dtype=torch.int32, device=cuda_device)
+    csa.topk(p, torch.from_numpy(s).to(cuda_device), q_pos0, idx)
+    ref = O.topk(s[0].astype(np.float64), np.array([q_pos0]), m, k)
+    assert np.array_equal(idx[0].cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("case", ["prefill_bf16_ragged", "decode_mixed", "tiny_f32"])
