@@ -736,17 +736,21 @@ int max_tiles(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0)
 
 // Split plan of the tensor-core path: one split per (query, half) for
 // multi-query launches; decode (one query per sequence) cuts the key list
-// into at most 16 runs of equal tile counts.  Depends on Q and the key-list
-// length only.
+// into runs of kDecodeTiles tiles (more when that would exceed 16 runs), so
+// a CTA pipelines several tiles and writes one partial for them.  Depends on
+// Q and the key-list length only, never on the batch.
+constexpr int kDecodeTiles = 5;
+
 void attend_tc_plan(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0, int* splits,
                     int* tps) {
   const int nt = max_tiles(p, Q, N, dense, q_pos0);
-  if (Q > 1 || nt <= 1) {
+  if (Q > 1 || nt <= kDecodeTiles) {
     *splits = 1;
     *tps = nt > 0 ? nt : 1;
     return;
   }
-  const int t = (int)ceil_div(nt, 16);
+  int t = (int)ceil_div(nt, 16);
+  if (t < kDecodeTiles) t = kDecodeTiles;
   *tps = t;
   *splits = (int)ceil_div(nt, t);
 }

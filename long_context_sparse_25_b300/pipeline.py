@@ -88,8 +88,8 @@ class Step:
         else:
             kd = wl.k
         n_keys = ((kd + 3) // 4) * 4 + wl.W
-        if tc:
-            attend = 1 + (1 if (wl.Q == 1 and n_keys > 128) else 0)
+        if tc:  # decode splits the key list once it exceeds 5 tiles of 128 keys
+            attend = 1 + (1 if (wl.Q == 1 and -(-n_keys // 128) > 5) else 0)
         else:
             attend = 1 + (1 if (rows < 1024 and kd + wl.W > 128) else 0)
         if wl.mode.startswith("hca"):
