@@ -135,10 +135,12 @@ def _config(wl):
                        f"Q={wl.Q} per sequence, k={wl.k}, H={wl.H}, D={wl.D_v}+{wl.D_qk - wl.D_v}, "
                        f"indexer {wl.H_I}x{wl.d_I}, window {wl.W}, {wl.dtype}",
            "B": wl.B, "context": wl.L, "entries": wl.N, "queries_per_seq": wl.Q, "k": wl.k}
-    if wl.mode == "csa_decode":
-        cfg["l2"] = "inputs larger than L2 (2.2 GB streamed per step > 126 MB), no flush"
-    else:
-        cfg["l2"] = "inputs larger than L2 (9.7 GB of queries, 4.3 GB of scores per step), no flush"
+    w = algorithmic_work(wl)
+    streamed = sum(v for k, v in w.items() if k.endswith("_bytes"))
+    if wl.mode == "csa_prefill":
+        streamed += wl.B * wl.Q * wl.N * 4  # the score matrix, written and read back
+    cfg["l2"] = (f"inputs larger than L2 ({streamed / 1e9:.2f} GB streamed per step > 126 MB), "
+                 "no flush")
     return cfg
 
 
@@ -221,18 +223,30 @@ def algorithmic_work(wl):
     nv = np.minimum((t + 1) // m, N)
     win = np.minimum(wl.W, t + 1)
     esz = 2
+    mixed = wl.dtype == "mixed"
+    # bytes of one stored entry / indexer key (mixed: e4m3 codes + fp32 scale, bf16 RoPE dims)
+    entry_b = (wl.D_v + 4 + (wl.D_qk - wl.D_v) * 2) if mixed else wl.D_qk * esz
+    key_b = (wl.d_I + 4) if mixed else wl.d_I * esz
+    qi_b = (wl.H_I * (wl.d_I + 4)) if mixed else wl.H_I * wl.d_I * esz
+    decode = wl.mode.endswith("decode")
+    new = N - (N - 1 if decode else 0)
     w = {}
     if wl.mode.startswith("csa"):
-        new = N - (N - 1 if wl.mode.endswith("decode") else 0)
         # raw rows + gates in, entries out, for the KV and the indexer keys
-        w["compress_bytes"] = B * new * (m * 2 * (wl.D_qk + wl.d_I) * esz + (wl.D_qk + wl.d_I) * esz)
-        w["index_bytes"] = B * (N * wl.d_I * esz + wl.Q * (wl.H_I * wl.d_I * esz + wl.H_I * 4))
+        w["compress_bytes"] = B * new * (m * 2 * (wl.D_qk + wl.d_I) * esz + entry_b + key_b)
+        w["index_bytes"] = B * (N * key_b + wl.Q * (qi_b + wl.H_I * 4))
         w["index_flops"] = float(B * nv.sum() * wl.H_I * wl.d_I * 2)
         keys = np.minimum(wl.k, nv) + win
         w["attend_flops"] = float(B * keys.sum() * wl.H * (wl.D_qk + wl.D_v) * 2)
-        w["attend_bytes"] = B * (keys.sum() * wl.D_qk * esz
+        w["attend_bytes"] = B * (np.minimum(wl.k, nv).sum() * entry_b + win.sum() * wl.D_qk * esz
                                  + wl.Q * wl.H * (wl.D_qk + wl.D_v) * esz)
-    return w
+    else:  # HCA: every visible entry plus the window
+        w["compress_bytes"] = B * new * (m * 2 * wl.D_qk * esz + entry_b)
+        keys = nv + win
+        w["hca_flops"] = float(B * keys.sum() * wl.H * (wl.D_qk + wl.D_v) * 2)
+        w["hca_bytes"] = B * (N * entry_b + win.max() * wl.D_qk * esz
+                              + wl.Q * wl.H * (wl.D_qk + wl.D_v) * esz)
+    return {k: float(v) for k, v in w.items()}
 
 
 def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
@@ -249,14 +263,21 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     N = wl.N
     decode = wl.mode.endswith("decode")
     n0 = N - 1 if decode else 0
-    scores, sel = step.scores(), step.selected()
-    off = sel.data_ptr() - step.ws.data_ptr() + sel.numel() * 4
-    off = (off + 255) // 256 * 256
-    rest = step.ws[off:]
+    if wl.mode.startswith("csa"):
+        scores, sel = step.scores(), step.selected()
+        off = sel.data_ptr() - step.ws.data_ptr() + sel.numel() * 4
+        off = (off + 255) // 256 * 256
+        rest = step.ws[off:]
 
     # the step's C-ABI calls one by one (the kernels csa_forward launches),
     # each timed in a graph of its own
-    parts = {
+    hca_parts = {
+        "compress": lambda: csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, n0, N, step.kv,
+                                         x_pos0=wl.raw_pos0, stream=stream),
+        "hca": lambda: csa.hca(p, inp["q"], step.kv, step.raw, wl.raw_pos0, wl.q_pos0, N, step.out,
+                               ws=step.ws, stream=stream),
+    }
+    parts = hca_parts if wl.mode.startswith("hca") else {
         "compress": lambda: (csa.compress(inp["x"], inp["g"], inp["bias"], wl.m, n0, N, step.kv,
                                           x_pos0=wl.raw_pos0, stream=stream),
                              csa.compress(inp["xi"], inp["gi"], inp["bias_i"], wl.m, n0, N,
@@ -320,7 +341,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     per_part = {name: timed(g_, args.steps) / args.steps for name, g_ in g_part.items()}
 
     # end to end: the step's new inputs from pinned host memory, the output back
-    h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi")]
+    h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi") if k in inp]
     if "q_idx_scale" in inp:
         h2d.append(inp["q_idx_scale"])
     host_in = [t_.cpu().pin_memory() for t_ in h2d]
@@ -355,10 +376,26 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
 
 
 def roofline(wl, per_part, peaks, peak_kind):
-    """Roofline of the dominant part: HBM for the decode indexer stream, the
+    """Roofline of the dominant part: HBM for the decode streams (the CSA
+    indexer over the key cache, the HCA attention over the entry cache), the
     bf16 tensor peak for the prefill contractions (parts timed alone, so the
     burst peak applies)."""
     w = algorithmic_work(wl)
+    if wl.mode == "hca_decode":
+        name = "hca"
+        achieved = w["hca_bytes"] / (per_part[name] / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s", "frac": achieved / peak,
+                "traffic": _traffic(f"{name}:{wl.name}"), "algorithmic_bytes_per_launch": w["hca_bytes"],
+                "tensor_frac": w["hca_flops"] / (per_part[name] / 1e3) / 1e12 / peaks["bf16_tflops"]}
+    if wl.mode == "hca_prefill":
+        name = "hca"
+        achieved = w["hca_flops"] / (per_part[name] / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": _traffic(f"{name}:{wl.name}"), "algorithmic_flops_per_launch": w["hca_flops"]}
     if wl.mode == "csa_decode":
         name = "index"
         achieved = w["index_bytes"] / (per_part[name] / 1e3) / 1e9
@@ -393,16 +430,27 @@ def run_ours(args, wl):
     peaks, peak_kind = _peaks()
 
     head = measure(args, wl, dev, dist, world, rank)
+
+    def secondary(name, steps):
+        sw = synth.WORKLOADS[name]
+        sargs = argparse.Namespace(**vars(args))
+        sargs.steps = steps
+        r = measure(sargs, sw, dev, dist, world, rank, e2e_steps=min(steps, 5), with_clocks=False)
+        dec = sw.mode.endswith("decode")
+        return {"workload": _config(sw)["workload"], "value": r["value"],
+                "unit": "tok/s" if dec else "query-tok/s", "ms_per_step": r["ms"],
+                "steps": steps, "per_part_ms": r["per_part_ms"],
+                "roofline": roofline(sw, r["per_part_ms"], peaks, peak_kind),
+                "e2e": r["e2e"], "gpu_launches": r["launches_per_step"] * steps}
+
     prefill = None
+    others = {}
     if not args.no_prefill and wl.mode == "csa_decode":
-        pw = synth.WORKLOADS["csa_prefill_64k"]
-        pr = measure(args, pw, dev, dist, world, rank, e2e_steps=min(args.steps, 5),
-                     with_clocks=False)
-        prefill = {"workload": _config(pw)["workload"], "value": pr["value"],
-                   "unit": "query-tok/s", "ms_per_step": pr["ms"],
-                   "per_part_ms": pr["per_part_ms"],
-                   "roofline": roofline(pw, pr["per_part_ms"], peaks, peak_kind),
-                   "e2e": pr["e2e"], "gpu_launches": pr["launches_per_step"] * args.steps}
+        prefill = secondary("csa_prefill_64k", args.steps)
+        if not args.no_others:
+            # the other rows of the path: HCA prefill and decode, mixed-precision decode
+            for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k"):
+                others[name] = secondary(name, min(args.steps, 10))
 
     if rank != 0:
         if dist:
@@ -434,6 +482,7 @@ def run_ours(args, wl):
         "clocks": head["clocks"],
         "cpu_baseline": cpu,
         "prefill": prefill,
+        "others": others or None,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -449,7 +498,9 @@ def main():
     ap.add_argument("--workload", default="csa_decode_1m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
-                    help="skip the 64K-token prefill measurement")
+                    help="skip the secondary measurements (64K prefill and the others)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the HCA and mixed-precision measurements")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiler captures)")
     ap.add_argument("--context", type=int, default=None,

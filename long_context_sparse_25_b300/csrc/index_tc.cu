@@ -447,10 +447,20 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   a.b_chunk_bytes = NM * 128;
   a.a_bytes = a.a_chunk_bytes * a.n_chunks;
   a.b_bytes = a.b_chunk_bytes * a.n_chunks;
-  const size_t budget = 220 * 1024;
-  // two query buffers when that still leaves a ring of at least 4 key stages
-  a.nb = (2 * (size_t)a.b_bytes + 4 * (size_t)a.a_bytes <= budget - 1024) ? 2 : 1;
-  int stages = (int)((budget - 1024 - a.nb * (size_t)a.b_bytes) / a.a_bytes);
+  // The key stream is latency-bound (a key tile takes ~4 us from TMA issue to
+  // arrival under full load), so the ring takes all the shared memory that is
+  // left: 227 KB less the alignment pad, the barriers, the staged head
+  // weights and the query buffers (two when that still leaves 4 key stages).
+  const size_t wbytes = (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
+  const size_t fixed = 1024 + 9 * sizeof(uint64_t) + 16 + 16 + wbytes;
+  const size_t per_stage = a.a_bytes + 2 * sizeof(uint64_t);
+  const size_t limit = 227 * 1024;
+  auto stages_for = [&](int nb) {
+    const size_t used = fixed + (size_t)nb * a.b_bytes;
+    return used >= limit ? 0 : (int)((limit - used) / per_stage);
+  };
+  a.nb = stages_for(2) >= 4 ? 2 : 1;
+  int stages = stages_for(a.nb);
   if (stages > 8) stages = 8;
   if (stages < 2) return cudaErrorNotSupported;
   a.stages = stages;
