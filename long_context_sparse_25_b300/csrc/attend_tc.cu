@@ -179,21 +179,42 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 //         and RoPE dims as they are.
 enum ChunkMode { kHi = 0, kLo = 1, kVal = 2 };
 
-__device__ __forceinline__ uint4 manual_unit(const AttArgs& a, int64_t row, bool win, int c,
-                                             int uc, int mode) {
+// The raw 16 bytes (bf16 rows) or 8 bytes (e4m3 codes) of a unit, and the
+// row scale the codes need; split from the conversion so that a producer
+// thread can have all its loads of a chunk in flight at once.
+struct RawUnit {
+  uint4 v;
+  float sc;
+  int kind;  // 0: bf16 values, 1: e4m3 codes in v.x / v.y, 2: zeros
+};
+
+__device__ __forceinline__ RawUnit manual_load(const AttArgs& a, int64_t row, bool win, int c, int uc,
+                                               int mode) {
+  RawUnit r;
+  r.sc = 1.f;
   const int d0 = c * 64 + uc * 8;
-  if (win) {
-    if (mode == kLo) return make_uint4(0u, 0u, 0u, 0u);
-    return __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
+  if (win || d0 >= a.nope) {
+    r.kind = mode == kLo ? 2 : 0;
+    if (r.kind == 2) {
+      r.v = make_uint4(0u, 0u, 0u, 0u);
+    } else if (win) {
+      r.v = __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
+    } else {
+      const int rw = a.D_qk - a.nope;
+      r.v = __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
+    }
+    return r;
   }
-  if (d0 >= a.nope) {
-    if (mode == kLo) return make_uint4(0u, 0u, 0u, 0u);
-    const int rw = a.D_qk - a.nope;
-    return __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
-  }
+  r.kind = 1;
   const uint2 cv = __ldg(reinterpret_cast<const uint2*>(a.codes + row * a.nope + d0));
-  const float sc = mode == kVal ? 1.f : __ldg(a.kscale + row);
-  const uint32_t w2[2] = {cv.x, cv.y};
+  r.v = make_uint4(cv.x, cv.y, 0u, 0u);
+  if (mode != kVal) r.sc = __ldg(a.kscale + row);
+  return r;
+}
+
+__device__ __forceinline__ uint4 manual_convert(const RawUnit& r, int mode) {
+  if (r.kind != 1) return r.v;
+  const uint32_t w2[2] = {r.v.x, r.v.y};
   uint32_t o[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -201,8 +222,8 @@ __device__ __forceinline__ uint4 manual_unit(const AttArgs& a, int64_t row, bool
     const int sh = (e & 1) * 16;
     // code * scale in fp32 is within 2^-24 of the exact product; the high
     // part is its bf16 rounding, the low part the (exact) rest
-    float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * sc;
-    float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * sc;
+    float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * r.sc;
+    float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * r.sc;
     if (mode == kLo) {
       f0 -= __bfloat162float(__float2bfloat16_rn(f0));
       f1 -= __bfloat162float(__float2bfloat16_rn(f1));
@@ -314,15 +335,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) return false;
         const uint32_t dst = tc::smem_u32(sRing + slot * kChunk);
+        if (kE4M3) {
+          // every load of the chunk in flight first, then the conversions
+          RawUnit raw[kUnits];
 #pragma unroll
-        for (int i = 0; i < kUnits; ++i) {
-          const int unit = pt + kProd * i;
-          if (unit < (int)(kChunk / 16)) {
-            const int r = unit >> 3, uc = unit & 7;
-            if (kE4M3) {
-              const uint4 v = manual_unit(a, rr[i], (wb >> i) & 1, c, uc, mode);
-              *reinterpret_cast<uint4*>(sRing + slot * kChunk + swz(r, uc)) = v;
-            } else {
+          for (int i = 0; i < kUnits; ++i) {
+            const int unit = pt + kProd * i;
+            if (unit < (int)(kChunk / 16))
+              raw[i] = manual_load(a, rr[i], (wb >> i) & 1, c, unit & 7, mode);
+          }
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i) {
+            const int unit = pt + kProd * i;
+            if (unit < (int)(kChunk / 16))
+              *reinterpret_cast<uint4*>(sRing + slot * kChunk + swz(unit >> 3, unit & 7)) =
+                  manual_convert(raw[i], mode);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i) {
+            const int unit = pt + kProd * i;
+            if (unit < (int)(kChunk / 16)) {
+              const int r = unit >> 3, uc = unit & 7;
               const uint8_t* src = ((wb >> i) & 1 ? rawb : kvb) + rr[i] * rowb + c * 128 + uc * 16;
               cp_async16(dst + swz(r, uc), src);
             }

@@ -38,6 +38,46 @@ struct Vec<uint16_t, 8> {
     }
   }
 };
+// Packed form of VEC elements (kept packed while loads are in flight).
+template <typename T, int VEC>
+struct Packed;
+template <>
+struct Packed<float, 4> {
+  using type = float4;
+  __device__ static type load(const void* p, int64_t i) {
+    return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+  }
+  __device__ static void unpack(const type& v, float* o) {
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+};
+template <>
+struct Packed<uint16_t, 8> {
+  using type = uint4;
+  __device__ static type load(const void* p, int64_t i) {
+    return *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p) + i);
+  }
+  __device__ static void unpack(const type& v, float* o) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o[2 * j] = __uint_as_float(w[j] << 16);
+      o[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+};
+template <typename T>
+struct Packed<T, 1> {
+  using type = float;
+  __device__ static type load(const void* p, int64_t i) {
+    float o;
+    if constexpr (sizeof(T) == 4) o = reinterpret_cast<const float*>(p)[i];
+    else o = bf16_to_f32(reinterpret_cast<const uint16_t*>(p)[i]);
+    return o;
+  }
+  __device__ static void unpack(const type& v, float* o) { o[0] = v; }
+};
+
 template <typename T>
 struct Vec<T, 1> {
   __device__ static void load(const void* p, int64_t i, float* o) {
@@ -227,6 +267,57 @@ __global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ 
     // first raw row of the block, relative to the rows held in x / g
     const int64_t row0 = (int64_t)b * T_rows + s * m - row_off;
 
+    if (out_mode != 2 && m > 16) {
+      // one pass with a running maximum (large blocks: m' = 128 rows are read
+      // once, eight rows' loads in flight at a time); the result is rounded
+      // once, so no error bound is needed
+      float mx[VEC], S[VEC], A[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) { mx[v] = -INFINITY; S[v] = 0.f; A[v] = 0.f; }
+      using P = Packed<T, VEC>;
+      for (int i0 = 0; i0 < m; i0 += 8) {
+        typename P::type gp[8], xp[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          if (i0 + ii < m) {
+            gp[ii] = P::load(g, (row0 + i0 + ii) * C + c0);
+            xp[ii] = P::load(x, (row0 + i0 + ii) * C + c0);
+          }
+        }
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          if (i0 + ii < m) {
+            float gv[VEC], xv[VEC];
+            P::unpack(gp[ii], gv);
+            P::unpack(xp[ii], xv);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              const float z = gv[v] + bias[(i0 + ii) * C + c0 + v];
+              if (z > mx[v]) {  // rescale what has been summed so far
+                const float r = __expf(mx[v] - z);  // 0 for the first row
+                S[v] *= r;
+                A[v] *= r;
+                mx[v] = z;
+              }
+              const float e = __expf(z - mx[v]);
+              S[v] += e;
+              A[v] = fmaf(e, xv[v], A[v]);
+            }
+          }
+        }
+      }
+      const int64_t orow1 = (int64_t)b * out_rows + s;
+      if (out_mode == 0) {
+        float* o = reinterpret_cast<float*>(out) + orow1 * C + c0;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) o[v] = A[v] / S[v];
+      } else {
+        uint16_t* o = reinterpret_cast<uint16_t*>(out) + orow1 * C + c0;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) o[v] = __bfloat16_as_ushort(__float2bfloat16_rn(A[v] / S[v]));
+      }
+      continue;
+    }
     float mx[VEC], zabs[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) { mx[v] = -INFINITY; zabs[v] = 0.f; }

@@ -461,7 +461,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   };
   a.nb = stages_for(2) >= 4 ? 2 : 1;
   int stages = stages_for(a.nb);
-  if (stages > 8) stages = 8;
+  if (stages > 16) stages = 16;
   if (stages < 2) return cudaErrorNotSupported;
   a.stages = stages;
   a.tmem_cols = (uint32_t)pow2_at_least(2 * NM);
