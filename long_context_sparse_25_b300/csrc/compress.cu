@@ -90,7 +90,7 @@ struct Vec<T, 1> {
 // the double-float evaluation below cannot place on one side of a bfloat16
 // rounding boundary (float64 is slow on this part, so it must stay rare).
 template <typename T>
-__device__ double pool_f64(const void* x, const void* g, const float* bias, int64_t row0, int C,
+__device__ __noinline__ double pool_f64(const void* x, const void* g, const float* bias, int64_t row0, int C,
                            int m, int c) {
   double mx = -INFINITY;
   for (int i = 0; i < m; ++i) {
@@ -189,7 +189,7 @@ __device__ ff ff_exp_nonpos(ff d) {
   const ff kl = ff_fast_two_sum(p, fmaf(k, ln2_hi, -p) + k * ln2_lo);
   const ff r = ff_add(d, ff{-kl.hi, -kl.lo});
   ff s{c_inv_fact[13][0], c_inv_fact[13][1]};
-#pragma unroll
+#pragma unroll 1
   for (int n = 12; n >= 0; --n) s = ff_add(ff_mul(s, r), ff{c_inv_fact[n][0], c_inv_fact[n][1]});
   const int ki = (int)k;
   return ff{ldexpf(s.hi, ki), ldexpf(s.lo, ki)};
@@ -229,8 +229,12 @@ __device__ ff pool_ff(const void* x, const void* g, const float* bias, int64_t r
 // midpoint (every other float is a full float ulp away from the nearest
 // midpoint); then the sign of lo decides, and a lo too small to trust sends
 // the channel to float64.
+//
+// Compiled once (not inlined, its loops rolled): a few lanes of a warp take
+// this path, and an inlined copy per unrolled channel left them waiting on
+// instruction fetches through long stretches of cold code.
 template <typename T>
-__device__ uint16_t pool_bf16_exact(const void* x, const void* g, const float* bias, int64_t row0,
+__device__ __noinline__ uint16_t pool_bf16_exact(const void* x, const void* g, const float* bias, int64_t row0,
                                     int C, int m, int c) {
   float mag = 0.f;
   const ff v = pool_ff<T>(x, g, bias, row0, C, m, c, &mag);

@@ -35,13 +35,14 @@ namespace {
 __device__ int g_index_tc_error = 0;
 
 constexpr int kTileKeys = 128;
+constexpr int kMaxAcc = 8;  // accumulator buffers in TMEM (up to 512 columns)
 
 struct TcArgs {
   int B, Q, H_I, d_I, m, NQ, nQB, tps;  // tps: key tiles per sequence (all N)
   int64_t N, n_rows, q_pos0;
   int mode;                             // 0: every query block sees all tiles; 1: causal units
   int64_t total;                        // mode 0: B*nQB*tps tiles; mode 1: B*nQB units
-  int stages, nb;
+  int stages, nb, nacc;  // nacc: TMEM accumulator buffers, a power of two
   uint32_t a_bytes, b_bytes, a_chunk_bytes, b_chunk_bytes;
   int chunk_elems, n_chunks, ksteps;
   uint32_t tmem_cols;
@@ -120,6 +121,23 @@ struct Sched {
   }
 };
 
+// The MMAs of one key tile: K steps of 32 bytes (16 bf16 or 32 e4m3), four
+// per 128-byte swizzled chunk.  A descriptor is advanced by adding the byte
+// offset / 16 to its start-address field, so the unrolled loop spends a couple
+// of integer adds per MMA: the single issuing thread would otherwise take
+// longer to build descriptors than the tensor core takes for an N = 64 MMA.
+template <int KSTEPS, bool kFP8>
+__device__ __forceinline__ void issue_tile(uint32_t d, uint64_t ad, uint64_t bd, uint32_t b_chunk16,
+                                           uint32_t id) {
+#pragma unroll
+  for (int kk = 0; kk < KSTEPS; ++kk) {
+    const uint64_t a_k = ad + (uint64_t)((kk >> 2) * ((kTileKeys * 128) >> 4) + (kk & 3) * 2);
+    const uint64_t b_k = bd + (uint64_t)((kk >> 2) * b_chunk16 + (kk & 3) * 2);
+    if (kFP8) tc::mma_e4m3(d, a_k, b_k, id, kk > 0 ? 1u : 0u);
+    else tc::mma_bf16(d, a_k, b_k, id, kk > 0 ? 1u : 0u);
+  }
+}
+
 template <bool kFP8, int kEpiWG>
 __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     index_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
@@ -135,8 +153,8 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
   uint64_t* b_full = bars + 2 * a.stages;
   uint64_t* b_empty = b_full + 2;
   uint64_t* acc_full = b_empty + 2;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* mma_done = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kMaxAcc;
+  uint64_t* mma_done = acc_empty + kMaxAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   // [epilogue warps][QPW * H_I], read as float4: 16-byte aligned
   float* a_w_smem = reinterpret_cast<float*>(
@@ -154,6 +172,8 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&b_full[s], 1);
       tc::mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < a.nacc; ++s) {
       tc::mbar_init(&acc_full[s], 1);
       tc::mbar_init(&acc_empty[s], 4 * kEpiWG);
     }
@@ -209,9 +229,15 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t id = kFP8 ? tc::idesc(kTileKeys, NM, 0, 0) : tc::idesc(kTileKeys, NM, 1, 1);
-      const int kstep_bytes = 32;  // 16 bf16 or 32 e4m3 per MMA
-      const int steps_per_chunk = 128 / kstep_bytes;
-      uint32_t it = 0, qcount = 0, acc_it = 0, bi = 0;
+      // descriptors of stage 0 / query buffer 0; the others are whole-buffer
+      // offsets in the start-address field (shared memory stays below 256 KB)
+      const uint64_t ad0 = tc::sdesc_sw128(tc::smem_u32(sA));
+      const uint64_t bd0 = tc::sdesc_sw128(tc::smem_u32(sB));
+      const uint32_t a_stage16 = a.a_bytes >> 4, b_buf16 = a.b_bytes >> 4;
+      const uint32_t b_chunk16 = a.b_chunk_bytes >> 4;
+      uint32_t s = 0, s_ph = 0;      // ring stage and the parity of its fill
+      uint32_t acc = 0, acc_ph = 0;  // accumulator buffer and its parity
+      uint32_t qcount = 0, bi = 0;
       int pb = -1, pqb = -1;
       bool ok = true;
       while (ok && sch.next(b, qb, kt)) {
@@ -223,25 +249,21 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
           pb = b;
           pqb = qb;
         }
-        const uint32_t s = it % a.stages;
-        if (!tc::mbar_wait(&a_full[s], (it / a.stages) & 1, err, 4)) { ok = false; break; }
-        const uint32_t acc = acc_it & 1;
-        if (!tc::mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, err, 5)) { ok = false; break; }
+        if (!tc::mbar_wait(&a_full[s], s_ph, err, 4)) { ok = false; break; }
+        if (!tc::mbar_wait(&acc_empty[acc], acc_ph ^ 1, err, 5)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem_base + acc * NM;
-        const uint32_t a0 = tc::smem_u32(sA + s * a.a_bytes);
-        const uint32_t b0 = tc::smem_u32(sB + bi * a.b_bytes);
-        for (int kk = 0; kk < a.ksteps; ++kk) {
-          const int ch = kk / steps_per_chunk, off = (kk % steps_per_chunk) * kstep_bytes;
-          const uint64_t ad = tc::sdesc_sw128(a0 + ch * a.a_chunk_bytes + off);
-          const uint64_t bd = tc::sdesc_sw128(b0 + ch * a.b_chunk_bytes + off);
-          if (kFP8) tc::mma_e4m3(d, ad, bd, id, kk > 0);
-          else tc::mma_bf16(d, ad, bd, id, kk > 0);
+        const uint64_t ad = ad0 + s * a_stage16, bd = bd0 + bi * b_buf16;
+        switch (a.ksteps) {
+          case 4: issue_tile<4, kFP8>(d, ad, bd, b_chunk16, id); break;
+          case 8: issue_tile<8, kFP8>(d, ad, bd, b_chunk16, id); break;
+          case 12: issue_tile<12, kFP8>(d, ad, bd, b_chunk16, id); break;
+          default: issue_tile<16, kFP8>(d, ad, bd, b_chunk16, id); break;
         }
         tc::mma_commit(&a_empty[s]);
         tc::mma_commit(&acc_full[acc]);
-        ++it;
-        ++acc_it;
+        if (++s == (uint32_t)a.stages) { s = 0; s_ph ^= 1; }
+        if (++acc == (uint32_t)a.nacc) { acc = 0; acc_ph ^= 1; }
       }
       // every MMA issued must have completed before TMEM is released
       tc::mma_commit(mma_done);
@@ -259,7 +281,13 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     float* sw = a_w_smem + (size_t)ew * QPW * a.H_I;
     uint32_t acc_it = 0;
     int cur_b = -1, cur_qb = -1;
+    int64_t nv_q[4] = {0, 0, 0, 0};  // visible entries of this warpgroup's queries
     while (sch.next(b, qb, kt)) {
+      const int64_t s = (int64_t)kt * kTileKeys + row;
+      // the e4m3 key scale is fetched before the accumulator wait (its
+      // latency would otherwise sit on the epilogue's critical path)
+      float ks = 1.f;
+      if (kFP8 && s < a.N) ks = __ldg(a.k_scale + (int64_t)b * a.n_rows + s);
       if (b != cur_b || qb != cur_qb) {
         // stage w (times the e4m3 query-row scale) once per query block
         __syncwarp();
@@ -273,12 +301,17 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
           sw[e] = wj;
         }
         __syncwarp();
+        for (int ql = 0; ql < QPW; ++ql) {
+          const int i = qb * a.NQ + wg * QPW + ql;
+          const int64_t nv = i < a.Q ? n_vis(a.q_pos0 + i, a.m) : 0;
+          nv_q[ql] = nv > a.N ? a.N : nv;
+        }
         cur_b = b;
         cur_qb = qb;
       }
-      const uint32_t acc = acc_it & 1;
+      const uint32_t acc = acc_it & (a.nacc - 1);
       // one lane waits, the warp follows converged (tcgen05.ld is .sync.aligned)
-      int okw = lane == 0 ? (int)tc::mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, err, 6) : 0;
+      int okw = lane == 0 ? (int)tc::mbar_wait(&acc_full[acc], (acc_it / a.nacc) & 1, err, 6) : 0;
       okw = __shfl_sync(0xffffffffu, okw, 0);
       __syncwarp();
       if (!okw) break;
@@ -319,16 +352,11 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
-      const int64_t s = (int64_t)kt * kTileKeys + row;
       if (s < a.N) {
-        float ks = 1.f;
-        if (kFP8) ks = __ldg(a.k_scale + (int64_t)b * a.n_rows + s);
         for (int ql = 0; ql < QPW; ++ql) {
           const int i = qb * a.NQ + wg * QPW + ql;
           if (i >= a.Q) break;
-          int64_t nv = n_vis(a.q_pos0 + i, a.m);
-          if (nv > a.N) nv = a.N;
-          a.scores[((int64_t)b * a.Q + i) * a.N + s] = s < nv ? sc[ql] * ks : -INFINITY;
+          a.scores[((int64_t)b * a.Q + i) * a.N + s] = s < nv_q[ql] ? sc[ql] * ks : -INFINITY;
         }
       }
       ++acc_it;
@@ -452,7 +480,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   // left: 227 KB less the alignment pad, the barriers, the staged head
   // weights and the query buffers (two when that still leaves 4 key stages).
   const size_t wbytes = (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
-  const size_t fixed = 1024 + 9 * sizeof(uint64_t) + 16 + 16 + wbytes;
+  const size_t fixed = 1024 + (5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 + wbytes;
   const size_t per_stage = a.a_bytes + 2 * sizeof(uint64_t);
   const size_t limit = 227 * 1024;
   auto stages_for = [&](int nb) {
@@ -464,7 +492,12 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   if (stages > 16) stages = 16;
   if (stages < 2) return cudaErrorNotSupported;
   a.stages = stages;
-  a.tmem_cols = (uint32_t)pow2_at_least(2 * NM);
+  // as many accumulator buffers as TMEM holds (at least two): the MMA of a
+  // key tile then never waits for the epilogue of an earlier one, so each
+  // ring stage is released as soon as its MMA has read it
+  a.nacc = 2;
+  while (a.nacc < kMaxAcc && 2 * a.nacc * NM <= 512) a.nacc *= 2;
+  a.tmem_cols = (uint32_t)pow2_at_least(a.nacc * NM);
   if (a.tmem_cols > 512) return cudaErrorNotSupported;
   const bool all_visible = n_vis(q_pos0, p.m) >= N;
   a.mode = all_visible ? 0 : 1;
@@ -486,7 +519,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   if (a.total < grid) grid = a.total;
   if (grid < 1) grid = 1;
   const size_t smem = 1024 + (size_t)a.stages * a.a_bytes + (size_t)a.nb * a.b_bytes +
-                      (2 * a.stages + 9) * sizeof(uint64_t) + 16 + 16 +
+                      (2 * a.stages + 5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 +
                       (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
   const int threads = 64 + 128 * epi_wg;
   cudaError_t e;
