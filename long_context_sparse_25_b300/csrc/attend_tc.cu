@@ -26,10 +26,11 @@
 // keys and then, one tile later, the D_v/128 chunks of the value half, with
 // 16-byte cp.async copies: each lane computes its own gathered row address
 // and swizzled destination (TMA gathers take their operands from warp-uniform
-// registers, so 32 lanes with 32 different rows serialise).  A thread keeps
-// kInFlight chunks in flight; once one has landed it issues a proxy fence
-// (its writes become visible to the tensor cores) and arrives on the chunk's
-// barrier.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims in
+// registers, so 32 lanes with 32 different rows serialise).  Each thread's
+// copies of a chunk arrive on the chunk's barrier by themselves once they
+// have landed (cp.async.mbarrier.arrive), so the producers run ahead as far
+// as the ring allows; the MMA issuer, after its wait, issues the proxy fence
+// that makes the rows visible to the tensor cores.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims in
 // bf16) are converted by the producers themselves: for QK^T each dequantised
 // key is split exactly into a bf16 high part and a bf16 low part (two chunk
 // loads per nope chunk, both multiplied by the same Q chunk), so the scores
@@ -72,7 +73,6 @@ constexpr int kProd = kProdWarps * 32;
 constexpr int kUnits = (kChunk / 16 + kProd - 1) / kProd;  // 16-byte units per producer thread
 constexpr int kMmaWarp = 3;          // warp 3: TMEM allocator + MMA issuer
 constexpr int kThreads = 256;        // + warps 4-7: softmax / epilogue
-constexpr int kInFlight = 3;         // cp.async chunk groups a producer thread keeps in flight
 
 struct AttArgs {
   int B, Q, H, D_qk, D_v, k, W, m;
@@ -130,8 +130,17 @@ struct SlotSrc {
   bool valid;
 };
 
-__device__ __forceinline__ SlotSrc slot_src(const AttArgs& a, const KeyList& kl, int b,
-                                            int64_t qrow, int j) {
+// The index-list word of key slot j (only selected-entry slots read the list;
+// the others return 0 and are resolved by slot_src from the slot number).
+__device__ __forceinline__ int32_t slot_word(const AttArgs& a, const KeyList& kl, int64_t qrow,
+                                             int j) {
+  if ((j < kl.k_ent || a.W == 0) && j < kl.kd && !a.dense) return a.idx[qrow * (int64_t)a.k + j];
+  return 0;
+}
+
+// `word`: slot_word of the same slot (fetched ahead of use).
+__device__ __forceinline__ SlotSrc slot_src(const AttArgs& a, const KeyList& kl, int b, int j,
+                                            int32_t word) {
   SlotSrc r;
   if (j < kl.k_ent || a.W == 0) {
     int64_t e = 0;
@@ -141,7 +150,7 @@ __device__ __forceinline__ SlotSrc slot_src(const AttArgs& a, const KeyList& kl,
         e = j;
         v = true;
       } else {
-        e = a.idx[qrow * (int64_t)a.k + j];
+        e = word;
         v = e >= 0 && e < a.N;  // -1 (and anything out of range) is an empty slot
         if (!v) e = 0;
       }
@@ -236,8 +245,11 @@ __device__ __forceinline__ uint4 manual_convert(const RawUnit& r, int mode) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
+// Arrive on `bar` (without raising its expected count) once every cp.async
+// this thread has issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar))
+               : "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -313,9 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producers
     // Thread pt copies the 16-byte units pt + kProd*i of every chunk (unit u:
     // row u/8, bytes 16*(u%8) of the row) with cp.async, each lane with its
-    // own gathered address, keeps kInFlight chunks in flight, and for each
-    // chunk that has landed makes its writes visible to the tensor cores
-    // (proxy fence) before arriving.
+    // own gathered address.  Each thread's copies of a chunk arrive on the
+    // chunk's barrier by themselves when they land (cp.async.mbarrier.arrive),
+    // so a producer never waits for its own copies: it runs ahead as far as
+    // the ring lets it, and the MMA issuer makes the landed rows visible to
+    // the tensor cores (proxy fence) after its wait.  The key-list words of
+    // the next tile are fetched a whole tile ahead.
     const int pt = threadIdx.x;
     if (n > 0) {
       if (pt == 0) {
@@ -326,15 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv16);
       const uint8_t* rawb = reinterpret_cast<const uint8_t*>(a.raw16);
       const int64_t rowb = (int64_t)a.D_qk * 2;
-      uint32_t lt = 0, pend = 0;
+      uint32_t pslot = 0, pph = 0;  // ring slot and the parity of its release
       bool ok = true;
       auto issue_chunk = [&](int c, int mode, const int64_t (&rr)[kUnits], uint32_t wb) -> bool {
-        const uint32_t slot = lt % kRing;
         int okw = 1;
-        if (lane == 0) okw = tc::mbar_wait(&ring_empty[slot], ((lt / kRing) & 1) ^ 1, err, 11);
+        if (lane == 0) okw = tc::mbar_wait(&ring_empty[pslot], pph ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) return false;
-        const uint32_t dst = tc::smem_u32(sRing + slot * kChunk);
+        const uint32_t dst = tc::smem_u32(sRing + pslot * kChunk);
         if (kE4M3) {
           // every load of the chunk in flight first, then the conversions
           RawUnit raw[kUnits];
@@ -348,9 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
-              *reinterpret_cast<uint4*>(sRing + slot * kChunk + swz(unit >> 3, unit & 7)) =
+              *reinterpret_cast<uint4*>(sRing + pslot * kChunk + swz(unit >> 3, unit & 7)) =
                   manual_convert(raw[i], mode);
           }
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(&ring_full[pslot]);
         } else {
 #pragma unroll
           for (int i = 0; i < kUnits; ++i) {
@@ -361,20 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               cp_async16(dst + swz(r, uc), src);
             }
           }
+          cp_async_arrive_noinc(&ring_full[pslot]);
         }
-        if (kE4M3) {
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive(&ring_full[slot]);
-        } else {
-          cp_async_commit();
-          if (++pend > (uint32_t)kInFlight) {
-            cp_async_wait<kInFlight>();
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&ring_full[(lt - kInFlight) % kRing]);
-            --pend;
-          }
+        if (++pslot == kRing) {
+          pslot = 0;
+          pph ^= 1;
         }
-        ++lt;
         return true;
       };
       // gathered rows of tile u's units, and the two mask slots of each thread
@@ -383,24 +391,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t wb;
         SlotSrc s0, s1;
       };
+      // key-list words of a tile's slots for this thread (units, then the two
+      // mask slots), fetched ahead of tile_rows
+      struct TileWords {
+        int32_t w[kUnits + 2];
+      };
       const bool has1 = pt + kProd < kT;
-      auto tile_rows = [&](int u, TileRows& t) {
+      auto tile_words = [&](int u, TileWords& t) {
+        const int jt = (tile0 + u) * kT;
+#pragma unroll
+        for (int i = 0; i < kUnits; ++i) {
+          const int unit = pt + kProd * i;
+          const int r = unit < (int)(kChunk / 16) ? unit >> 3 : 0;
+          t.w[i] = slot_word(a, kl, qrow, jt + r);
+        }
+        t.w[kUnits] = slot_word(a, kl, qrow, jt + pt);
+        t.w[kUnits + 1] = slot_word(a, kl, qrow, jt + (has1 ? pt + kProd : pt));
+      };
+      auto tile_rows = [&](int u, const TileWords& tw, TileRows& t) {
         const int jt = (tile0 + u) * kT;
         t.wb = 0;
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
           const int unit = pt + kProd * i;
           const int r = unit < (int)(kChunk / 16) ? unit >> 3 : 0;
-          const SlotSrc ss = slot_src(a, kl, b, qrow, jt + r);
+          const SlotSrc ss = slot_src(a, kl, b, jt + r, tw.w[i]);
           t.rr[i] = ss.row;
           t.wb |= (ss.win ? 1u : 0u) << i;
         }
-        t.s0 = slot_src(a, kl, b, qrow, jt + pt);
-        t.s1 = slot_src(a, kl, b, qrow, jt + (has1 ? pt + kProd : pt));
+        t.s0 = slot_src(a, kl, b, jt + pt, tw.w[kUnits]);
+        t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[kUnits + 1]);
       };
-      TileRows cur, nxt, prev;
-      tile_rows(0, cur);
+      TileRows cur, prev;
+      TileWords wnext;
+      tile_words(0, wnext);
+      tile_rows(0, wnext, cur);
       for (int u = 0; u <= n && ok; ++u) {
+        if (u + 1 < n) tile_words(u + 1, wnext);  // in flight during this tile's issues
         if (u < n) {
           // validity of slots pt and pt + 96 (and, for mixed caches, the scale
           // of their value rows) for the softmax: ballot word w covers slots
@@ -427,23 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < a.nsc && ok; ++cc)
             ok = cc < a.nc ? issue_chunk(cc, kHi, cur.rr, cur.wb)
                            : issue_chunk(cc - a.nc, kLo, cur.rr, cur.wb);
-          // the next tile's rows are looked up before the value chunks of the
-          // previous tile go out, so their arrivals (deferred to the next
-          // issues) do not wait on the index-list loads
-          if (u + 1 < n) tile_rows(u + 1, nxt);
         }
         if (u >= 1)
           for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev.rr, prev.wb);
         prev = cur;
-        cur = nxt;
+        if (u + 1 < n) tile_rows(u + 1, wnext, cur);
       }
-      // every copy must land before the CTA can exit; arrive for the chunks
-      // still pending
+      // every copy must land before the CTA can exit (their arrivals on the
+      // ring barriers happen by themselves)
       cp_async_wait<0>();
-      if (!kE4M3) {
-        tc::fence_proxy_async_smem();
-        for (uint32_t j = lt - pend; j < lt; ++j) tc::mbar_arrive(&ring_full[j % kRing]);
-      }
       if (pt == 0) tc::mbar_drain(q_full, 0);
     }
   } else if (warp == kMmaWarp) {
@@ -451,45 +470,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n > 0) {
       const uint32_t id_s = tc::idesc(128, kT, 1, 1);
       const uint32_t id_pv = tc::idesc(128, 64, 1, 1, 0, 1);
-      uint32_t lt = 0;
       bool ok = tc::mbar_wait(q_full, 0, err, 21);
-      const uint32_t q0 = tc::smem_u32(sQ);
-      const uint32_t r0 = tc::smem_u32(sRing);
+      // descriptors of Q chunk 0 and ring slot 0 (K-major for S, MN-major
+      // for PV); other chunks / slots / K steps are constant offsets in the
+      // start-address field, so each MMA costs the issuing thread a couple of
+      // integer adds (building descriptors per MMA made this loop, not the
+      // tensor core, the limit)
+      const uint64_t qd0 = tc::sdesc_sw128(tc::smem_u32(sQ));
+      const uint64_t rd0 = tc::sdesc_sw128(tc::smem_u32(sRing));
+      const uint64_t vd0 = tc::sdesc_sw128_mn(tc::smem_u32(sRing));
+      constexpr uint32_t kChunk16 = kChunk >> 4;
+      uint32_t slot = 0, ph = 0;  // ring slot and the parity of its fill
+      auto next_slot = [&]() {
+        if (++slot == kRing) {
+          slot = 0;
+          ph ^= 1;
+        }
+      };
       auto issue_pv = [&](int u) -> bool {
         const uint32_t sb = u & 1;
         if (!tc::mbar_wait(&p_full[sb], (u >> 1) & 1, err, 22)) return false;
         tc::tc_fence_after();
+        const uint32_t p_tmem = tmem + sb * 128;
         for (int c = 0; c < a.nvc; ++c) {
-          const uint32_t slot = lt % kRing;
-          if (!tc::mbar_wait(&ring_full[slot], (lt / kRing) & 1, err, 23)) return false;
+          if (!tc::mbar_wait(&ring_full[slot], ph, err, 23)) return false;
+          if (!kE4M3) tc::fence_proxy_async_smem();  // cp.async rows -> tensor cores
           tc::tc_fence_after();
+          const uint64_t vd = vd0 + slot * kChunk16;
+          const uint32_t o_tmem = tmem + 256 + 64 * c;
+#pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks) {
-            const uint64_t bd = tc::sdesc_sw128_mn(r0 + slot * kChunk + ks * 2048);
-            tc::mma_bf16_ts(tmem + 256 + 64 * c, tmem + sb * 128 + 8 * ks, bd, id_pv,
-                            (u > 0 || ks > 0) ? 1u : 0u);
+            // 16 keys per K step: 16 rows of 128 bytes
+            const uint64_t bd = vd + (uint64_t)(ks * (2048 >> 4));
+            tc::mma_bf16_ts(o_tmem, p_tmem + 8 * ks, bd, id_pv, (u > 0 || ks > 0) ? 1u : 0u);
             if (kE4M3)  // the low part of P
-              tc::mma_bf16_ts(tmem + 256 + 64 * c, tmem + sb * 128 + 64 + 8 * ks, bd, id_pv, 1u);
+              tc::mma_bf16_ts(o_tmem, p_tmem + 64 + 8 * ks, bd, id_pv, 1u);
           }
           tc::mma_commit(&ring_empty[slot]);
-          ++lt;
+          next_slot();
         }
         tc::mma_commit(&o_done[u & 1]);
         return true;
       };
       for (int u = 0; u < n && ok; ++u) {
         const uint32_t sb = u & 1;
+        const uint32_t s_tmem = tmem + sb * 128;
         for (int cc = 0; cc < a.nsc && ok; ++cc) {
           const int c = cc < a.nc ? cc : cc - a.nc;  // the Q chunk this key chunk meets
-          const uint32_t slot = lt % kRing;
-          if (!tc::mbar_wait(&ring_full[slot], (lt / kRing) & 1, err, 24)) { ok = false; break; }
+          if (!tc::mbar_wait(&ring_full[slot], ph, err, 24)) { ok = false; break; }
+          if (!kE4M3) tc::fence_proxy_async_smem();  // cp.async rows -> tensor cores
           tc::tc_fence_after();
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = tc::sdesc_sw128(q0 + c * kChunk + ks * 32);
-            const uint64_t bd = tc::sdesc_sw128(r0 + slot * kChunk + ks * 32);
-            tc::mma_bf16(tmem + sb * 128, ad, bd, id_s, (cc > 0 || ks > 0) ? 1u : 0u);
-          }
+          const uint64_t qd = qd0 + (uint32_t)c * kChunk16;
+          const uint64_t rd = rd0 + slot * kChunk16;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // 16 bf16 (32 bytes) per K step
+            tc::mma_bf16(s_tmem, qd + (uint64_t)(ks * 2), rd + (uint64_t)(ks * 2), id_s,
+                         (cc > 0 || ks > 0) ? 1u : 0u);
           tc::mma_commit(&ring_empty[slot]);
-          ++lt;
+          next_slot();
         }
         if (!ok) break;
         tc::mma_commit(&s_full[sb]);
