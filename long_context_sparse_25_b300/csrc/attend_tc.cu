@@ -343,7 +343,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rowb = (int64_t)a.D_qk * 2;
       uint32_t pslot = 0, pph = 0;  // ring slot and the parity of its release
       bool ok = true;
-      auto issue_chunk = [&](int c, int mode, const int64_t (&rr)[kUnits], uint32_t wb) -> bool {
+      // swizzled destination of each of this thread's units within a chunk;
+      // only the last unit can fall outside the chunk (threads pt >= 64)
+      uint32_t dso[kUnits];
+#pragma unroll
+      for (int i = 0; i < kUnits; ++i) {
+        const int unit = pt + kProd * i;
+        dso[i] = swz(unit >> 3, unit & 7);
+      }
+      const bool last_unit = pt + kProd * (kUnits - 1) < (int)(kChunk / 16);
+      // gathered rows of tile u's units (bf16 caches: the byte address of the
+      // unit in chunk 0; mixed caches: the row and its kind), and the two mask
+      // slots of each thread
+      struct TileRows {
+        int64_t rr[kUnits];
+        const uint8_t* sp[kUnits];
+        uint32_t wb;
+        SlotSrc s0, s1;
+      };
+      auto issue_chunk = [&](int c, int mode, const TileRows& t) -> bool {
         int okw = 1;
         if (lane == 0) okw = tc::mbar_wait(&ring_empty[pslot], pph ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -356,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
-              raw[i] = manual_load(a, rr[i], (wb >> i) & 1, c, unit & 7, mode);
+              raw[i] = manual_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7, mode);
           }
 #pragma unroll
           for (int i = 0; i < kUnits; ++i) {
@@ -368,15 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_proxy_async_smem();
           tc::mbar_arrive(&ring_full[pslot]);
         } else {
+          const int coff = c * 128;
 #pragma unroll
-          for (int i = 0; i < kUnits; ++i) {
-            const int unit = pt + kProd * i;
-            if (unit < (int)(kChunk / 16)) {
-              const int r = unit >> 3, uc = unit & 7;
-              const uint8_t* src = ((wb >> i) & 1 ? rawb : kvb) + rr[i] * rowb + c * 128 + uc * 16;
-              cp_async16(dst + swz(r, uc), src);
-            }
-          }
+          for (int i = 0; i < kUnits; ++i)
+            if (i < kUnits - 1 || last_unit) cp_async16(dst + dso[i], t.sp[i] + coff);
           cp_async_arrive_noinc(&ring_full[pslot]);
         }
         if (++pslot == kRing) {
@@ -384,12 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           pph ^= 1;
         }
         return true;
-      };
-      // gathered rows of tile u's units, and the two mask slots of each thread
-      struct TileRows {
-        int64_t rr[kUnits];
-        uint32_t wb;
-        SlotSrc s0, s1;
       };
       // key-list words of a tile's slots for this thread (units, then the two
       // mask slots), fetched ahead of tile_rows
@@ -418,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const SlotSrc ss = slot_src(a, kl, b, jt + r, tw.w[i]);
           t.rr[i] = ss.row;
           t.wb |= (ss.win ? 1u : 0u) << i;
+          t.sp[i] = (ss.win ? rawb : kvb) + ss.row * rowb + (unit & 7) * 16;
         }
         t.s0 = slot_src(a, kl, b, jt + pt, tw.w[kUnits]);
         t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[kUnits + 1]);
@@ -452,11 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
           for (int cc = 0; cc < a.nsc && ok; ++cc)
-            ok = cc < a.nc ? issue_chunk(cc, kHi, cur.rr, cur.wb)
-                           : issue_chunk(cc - a.nc, kLo, cur.rr, cur.wb);
+            ok = cc < a.nc ? issue_chunk(cc, kHi, cur) : issue_chunk(cc - a.nc, kLo, cur);
         }
         if (u >= 1)
-          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev.rr, prev.wb);
+          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev);
         prev = cur;
         if (u + 1 < n) tile_rows(u + 1, wnext, cur);
       }
