@@ -43,6 +43,7 @@ struct TcArgs {
   int mode;                             // 0: every query block sees all tiles; 1: causal units
   int64_t total;                        // mode 0: B*nQB*tps tiles; mode 1: B*nQB units
   int stages, nb, nacc;  // nacc: TMEM accumulator buffers, a power of two
+  int alt;               // 1: the two epilogue warpgroups take alternate tiles (all queries)
   uint32_t a_bytes, b_bytes, a_chunk_bytes, b_chunk_bytes;
   int chunk_elems, n_chunks, ksteps;
   uint32_t tmem_cols;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     }
     for (int s = 0; s < a.nacc; ++s) {
       tc::mbar_init(&acc_full[s], 1);
-      tc::mbar_init(&acc_empty[s], 4 * kEpiWG);
+      tc::mbar_init(&acc_empty[s], a.alt ? 4 : 4 * kEpiWG);
     }
     tc::mbar_init(mma_done, 1);
     tc::fence_mbar_init();
@@ -275,14 +276,22 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
     const int wg = ew >> 2;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
-    const int QPW = a.NQ / kEpiWG;  // queries per warpgroup
+    // queries per warpgroup and the first of them: the warpgroups split the
+    // queries of every tile, or (alt) take alternate tiles with all queries
+    const int QPW = a.alt ? a.NQ : a.NQ / kEpiWG;
+    const int qoff = a.alt ? 0 : wg * QPW;
     // this warp's copy of the head weights of its QPW queries (per-warp, so
     // no barrier across warps is needed)
     float* sw = a_w_smem + (size_t)ew * QPW * a.H_I;
     uint32_t acc_it = 0;
     int cur_b = -1, cur_qb = -1;
     int64_t nv_q[4] = {0, 0, 0, 0};  // visible entries of this warpgroup's queries
+    uint32_t tile_i = 0;
     while (sch.next(b, qb, kt)) {
+      if (a.alt && (int)(tile_i++ & 1) != wg) {  // the other warpgroup's tile
+        ++acc_it;
+        continue;
+      }
       const int64_t s = (int64_t)kt * kTileKeys + row;
       // the e4m3 key scale is fetched before the accumulator wait (its
       // latency would otherwise sit on the epilogue's critical path)
@@ -293,7 +302,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
         __syncwarp();
         for (int e = lane; e < QPW * a.H_I; e += 32) {
           const int ql = e / a.H_I, j = e - ql * a.H_I;
-          int i = qb * a.NQ + wg * QPW + ql;
+          int i = qb * a.NQ + qoff + ql;
           if (i >= a.Q) i = a.Q - 1;
           const int64_t wi = ((int64_t)b * a.Q + i) * a.H_I + j;
           float wj = __ldg(a.w + wi);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
         }
         __syncwarp();
         for (int ql = 0; ql < QPW; ++ql) {
-          const int i = qb * a.NQ + wg * QPW + ql;
+          const int i = qb * a.NQ + qoff + ql;
           const int64_t nv = i < a.Q ? n_vis(a.q_pos0 + i, a.m) : 0;
           nv_q[ql] = nv > a.N ? a.N : nv;
         }
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       tc::tc_fence_after();
       float sc[4];
       for (int ql = 0; ql < QPW; ++ql) {
-        const int qi = wg * QPW + ql;
+        const int qi = qoff + ql;
         const uint32_t col = acc * NM + qi * a.H_I;
         const float4* wq = reinterpret_cast<const float4*>(sw + ql * a.H_I);
         float part[4] = {0.f, 0.f, 0.f, 0.f};
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
       if (s < a.N) {
         for (int ql = 0; ql < QPW; ++ql) {
-          const int i = qb * a.NQ + wg * QPW + ql;
+          const int i = qb * a.NQ + qoff + ql;
           if (i >= a.Q) break;
           a.scores[((int64_t)b * a.Q + i) * a.N + s] = s < nv_q[ql] ? sc[ql] * ks : -INFINITY;
         }
@@ -466,7 +475,11 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   a.nQB = (Q + a.NQ - 1) / a.NQ;
   a.tps = (int)ceil_div(N, kTileKeys);
   const int NM = a.NQ * p.H_I;
-  const int epi_wg = (NM == 256 && a.NQ >= 2) ? 2 : 1;
+  // Two epilogue warpgroups: they split the queries of an N = 256 tile, or
+  // otherwise take alternate tiles (one warpgroup reducing a tile's heads is
+  // latency-bound and could not keep up with the key stream)
+  const int epi_wg = 2;
+  a.alt = (NM == 256 && a.NQ >= 2) ? 0 : 1;
   const int esz = fp8 ? 1 : 2;
   a.chunk_elems = 128 / esz;
   a.n_chunks = p.d_I * esz / 128;
@@ -479,7 +492,8 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   // arrival under full load), so the ring takes all the shared memory that is
   // left: 227 KB less the alignment pad, the barriers, the staged head
   // weights and the query buffers (two when that still leaves 4 key stages).
-  const size_t wbytes = (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
+  const size_t wbytes =
+      (size_t)4 * epi_wg * (a.alt ? a.NQ : a.NQ / epi_wg) * p.H_I * sizeof(float);
   const size_t fixed = 1024 + (5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 + wbytes;
   const size_t per_stage = a.a_bytes + 2 * sizeof(uint64_t);
   const size_t limit = 227 * 1024;
@@ -523,7 +537,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   if (grid < 1) grid = 1;
   const size_t smem = 1024 + (size_t)a.stages * a.a_bytes + (size_t)a.nb * a.b_bytes +
                       (2 * a.stages + 5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 +
-                      (size_t)4 * epi_wg * (a.NQ / epi_wg) * p.H_I * sizeof(float);
+                      wbytes;
   const int threads = 64 + 128 * epi_wg;
   cudaError_t e;
 #define CSA_LAUNCH_TC(FP8, EW)                                                                  \
