@@ -396,12 +396,10 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
 
   cudaError_t e;
   if (N > a->n_cached) {
-    e = launch_compress(a->x, a->gate, a->raw_dtype, a->bias, p->B, a->raw_pos0, a->R, p->m, p->D_qk,
-                        a->n_cached, N, a->kv, st);
-    if (e != cudaSuccess) return cuda_status(e, "csa_forward/compress kv");
-    e = launch_compress(a->xi, a->gate_i, a->raw_dtype, a->bias_i, p->B, a->raw_pos0, a->R, p->m,
-                        p->d_I, a->n_cached, N, a->keys, st);
-    if (e != cudaSuccess) return cuda_status(e, "csa_forward/compress keys");
+    e = launch_compress_pair(a->x, a->gate, a->bias, p->D_qk, a->kv, a->xi, a->gate_i, a->bias_i,
+                             p->d_I, a->keys, a->raw_dtype, p->B, a->raw_pos0, a->R, p->m,
+                             a->n_cached, N, st);
+    if (e != cudaSuccess) return cuda_status(e, "csa_forward/compress");
   }
   e = launch_index(*p, a->q_idx, a->q_idx_dtype, a->q_idx_scale, a->w, a->keys, a->q_pos0, a->Q, N,
                    scores, st, /*fill_invisible=*/false);

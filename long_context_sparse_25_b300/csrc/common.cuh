@@ -81,6 +81,13 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype, const float* bias,
                             int B, int64_t x_pos0, int64_t T, int m, int C, int64_t s_begin,
                             int64_t s_end, const csa_rows& out, cudaStream_t st);
+// The same blocks pooled into two caches (KV entries and indexer keys) in one
+// launch when both take the same kernel; otherwise two launches.
+cudaError_t launch_compress_pair(const void* x0, const void* g0, const float* bias0, int C0,
+                                 const csa_rows& out0, const void* x1, const void* g1,
+                                 const float* bias1, int C1, const csa_rows& out1,
+                                 csa_dtype in_dtype, int B, int64_t x_pos0, int64_t T, int m,
+                                 int64_t s_begin, int64_t s_end, cudaStream_t st);
 
 // fill_invisible: write -inf for entries beyond each query's visibility (the
 // fused forward skips it: top-k never reads them).

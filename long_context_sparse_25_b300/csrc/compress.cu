@@ -176,23 +176,37 @@ __constant__ float c_inv_fact[14][2] = {
     {1.6059044372074283e-10f, -5.352526511562726e-18f},
 };
 
-// e^d for d <= 0 in double-float: Cody-Waite reduction d = k ln2 + r
-// (|r| <= ln2/2, ln2 held as a double-float) and the Taylor series of e^r to
-// degree 13 (|r|^14/14! < 2^-50), evaluated in Horner form.
-__device__ ff ff_exp_nonpos(ff d) {
-  if (d.hi < -120.f) return ff{0.f, 0.f};  // below 2^-173: nothing next to the e^0 term
-  const float ln2_hi = 0.693147182464599609375f;        // float nearest to ln 2
-  const float ln2_lo = -1.904654323148236017e-09f;      // ln 2 - ln2_hi
-  const float k = rintf(d.hi * 1.44269504088896340736f);
-  // k * ln2 as a double-float: k * ln2_hi exactly (TwoProduct), plus k * ln2_lo
-  const float p = k * ln2_hi;
-  const ff kl = ff_fast_two_sum(p, fmaf(k, ln2_hi, -p) + k * ln2_lo);
-  const ff r = ff_add(d, ff{-kl.hi, -kl.lo});
-  ff s{c_inv_fact[13][0], c_inv_fact[13][1]};
+// e^d for four d <= 0 at once in double-float: for each, Cody-Waite
+// reduction d = k ln2 + r (|r| <= ln2/2, ln2 held as a double-float) and the
+// Taylor series of e^r to degree 13 (|r|^14/14! < 2^-50) in Horner form; the
+// four Horner chains are interleaved so that their latencies overlap.  Below
+// d = -120 (e^d < 2^-173, nothing next to the e^0 term) the result is 0.
+__device__ void ff_exp4_nonpos(const ff (&d)[4], ff (&e)[4]) {
+  const float ln2_hi = 0.693147182464599609375f;
+  const float ln2_lo = -1.904654323148236017e-09f;
+  ff r[4], s[4];
+  int ki[4];
+  bool zero[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    zero[j] = d[j].hi < -120.f;
+    const ff dj = zero[j] ? ff{0.f, 0.f} : d[j];
+    const float k = rintf(dj.hi * 1.44269504088896340736f);
+    const float p = k * ln2_hi;
+    const ff kl = ff_fast_two_sum(p, fmaf(k, ln2_hi, -p) + k * ln2_lo);
+    r[j] = ff_add(dj, ff{-kl.hi, -kl.lo});
+    s[j] = ff{c_inv_fact[13][0], c_inv_fact[13][1]};
+    ki[j] = (int)k;
+  }
 #pragma unroll 1
-  for (int n = 12; n >= 0; --n) s = ff_add(ff_mul(s, r), ff{c_inv_fact[n][0], c_inv_fact[n][1]});
-  const int ki = (int)k;
-  return ff{ldexpf(s.hi, ki), ldexpf(s.lo, ki)};
+  for (int n = 12; n >= 0; --n) {
+    const ff cn{c_inv_fact[n][0], c_inv_fact[n][1]};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = ff_add(ff_mul(s[j], r[j]), cn);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    e[j] = zero[j] ? ff{0.f, 0.f} : ff{ldexpf(s[j].hi, ki[j]), ldexpf(s[j].lo, ki[j])};
 }
 
 // Pooled value of one channel in double-float; *mag (if given) receives
@@ -208,15 +222,30 @@ __device__ ff pool_ff(const void* x, const void* g, const float* bias, int64_t r
     if (i == 0 || ff_gt(z, mx)) mx = z;
   }
   ff S{0.f, 0.f}, A{0.f, 0.f};
-  for (int i = 0; i < m; ++i) {
-    float gv, xv;
-    Vec<T, 1>::load(g, (row0 + i) * C + c, &gv);
-    Vec<T, 1>::load(x, (row0 + i) * C + c, &xv);
-    const ff z = ff_two_sum(gv, bias[i * C + c]);
-    const ff e = ff_exp_nonpos(ff_add(z, ff{-mx.hi, -mx.lo}));
-    S = ff_add(S, e);
-    A = ff_add(A, ff_mul_f(e, xv));
-    if (mag) *mag += e.hi * fabsf(xv);
+  for (int i0 = 0; i0 < m; i0 += 4) {  // four rows' exponentials at a time
+    ff d[4], e[4];
+    float xv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j;
+      xv[j] = 0.f;
+      d[j] = ff{-1000.f, 0.f};  // past the last row: e = 0, not summed
+      if (i < m) {
+        float gv;
+        Vec<T, 1>::load(g, (row0 + i) * C + c, &gv);
+        Vec<T, 1>::load(x, (row0 + i) * C + c, &xv[j]);
+        d[j] = ff_add(ff_two_sum(gv, bias[i * C + c]), ff{-mx.hi, -mx.lo});
+      }
+    }
+    ff_exp4_nonpos(d, e);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (i0 + j < m) {
+        S = ff_add(S, e[j]);
+        A = ff_add(A, ff_mul_f(e[j], xv[j]));
+        if (mag) *mag += e[j].hi * fabsf(xv[j]);
+      }
+    }
   }
   if (mag) *mag /= S.hi;
   return ff_div(A, S);
@@ -248,21 +277,36 @@ __device__ __noinline__ uint16_t pool_bf16_exact(const void* x, const void* g, c
   return ((v.lo > 0.f) == (v.hi > 0.f)) ? (uint16_t)(t + 1) : t;
 }
 
+// One pooling job: a set of rows (x, gates, position bias) of C channels
+// and the cache its entries go to.
 // out_mode: 0 = fp32 rows, 1 = bf16 rounded from the fp32 result,
 //           2 = bf16 nearest to the exact result (guard band + double-float
 //               recompute of the channels too close to a rounding boundary).
+struct CJob {
+  const void* x;
+  const void* g;
+  const float* bias;
+  int C;
+  void* out;
+  int64_t out_rows;
+  int out_mode;
+};
+
+// The items of one job, from `first`, every `stride`-th.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ x,
-                                                       const void* __restrict__ g,
-                                                       const float* __restrict__ bias, int B,
-                                                       int64_t T_rows, int64_t row_off, int m,
-                                                       int C, int64_t s_begin, int64_t n_s,
-                                                       void* __restrict__ out, int64_t out_rows,
-                                                       int out_mode) {
+__device__ __forceinline__ void pool_job(const CJob& J, int64_t first, int64_t stride, int B,
+                                         int64_t T_rows, int64_t row_off, int m, int64_t s_begin,
+                                         int64_t n_s) {
+  const void* __restrict__ x = J.x;
+  const void* __restrict__ g = J.g;
+  const float* __restrict__ bias = J.bias;
+  const int C = J.C;
+  void* __restrict__ out = J.out;
+  const int64_t out_rows = J.out_rows;
+  const int out_mode = J.out_mode;
   const int CV = C / VEC;
   const int64_t total = (int64_t)B * n_s * CV;
-  for (int64_t item = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; item < total;
-       item += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t item = first; item < total; item += stride) {
     const int cv = (int)(item % CV);
     const int64_t bs = item / CV;
     const int64_t s = s_begin + bs % n_s;
@@ -381,6 +425,23 @@ __global__ void __launch_bounds__(256) compress_kernel(const void* __restrict__ 
   }
 }
 
+// One launch for one or two jobs (a decode step pools its new entry for the
+// KV cache and for the indexer-key cache together): blocks [0, blocks0) take
+// job 0, the rest job 1, so a block's job is uniform.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) compress_kernel(const CJob j0, const CJob j1,
+                                                       unsigned blocks0, int B, int64_t T_rows,
+                                                       int64_t row_off, int m, int64_t s_begin,
+                                                       int64_t n_s) {
+  if (blockIdx.x < blocks0)
+    pool_job<T, VEC>(j0, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                     (int64_t)blocks0 * blockDim.x, B, T_rows, row_off, m, s_begin, n_s);
+  else
+    pool_job<T, VEC>(j1, (int64_t)(blockIdx.x - blocks0) * blockDim.x + threadIdx.x,
+                     (int64_t)(gridDim.x - blocks0) * blockDim.x, B, T_rows, row_off, m, s_begin,
+                     n_s);
+}
+
 // Mixed e4m3 + bf16 output: one block per entry; the pooled values in
 // double-float (exact in float64), then the row scale and the codes in float64.
 template <typename T>
@@ -426,6 +487,51 @@ __global__ void __launch_bounds__(256) compress_e4m3_kernel(
 
 }  // namespace
 
+// Channels per thread: 4 fp32 / 8 bf16 (16-byte loads) unless the step has
+// few entries (a decode step): then one channel per thread, so that the rare
+// channels needing the exact-rounding recompute sit in different threads (a
+// warp runs its lanes' recomputes one after another) and the grid is wider.
+static int pool_vec(csa_dtype in_dtype, int C, int B, int64_t n_s, int m) {
+  const bool few = (int64_t)B * n_s * m < 4096;
+  if (few) return 1;
+  if (in_dtype == CSA_F32) return C % 4 == 0 ? 4 : 1;
+  return C % 8 == 0 ? 8 : 1;
+}
+
+static cudaError_t launch_pool(const CJob& j0, const CJob& j1, csa_dtype in_dtype, int B,
+                               int64_t x_pos0, int64_t T, int m, int64_t s_begin, int64_t n_s,
+                               cudaStream_t st) {
+  const int vec = pool_vec(in_dtype, j0.C, B, n_s, m);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // blocks of each job: one item per thread, at most 16 blocks per SM in all
+  const int64_t items0 = (int64_t)B * n_s * (j0.C / vec), items1 = (int64_t)B * n_s * (j1.C / vec);
+  const int64_t cap = (int64_t)sms * 16;
+  int64_t b0 = ceil_div(items0, 256), b1 = ceil_div(items1, 256);
+  if (b0 + b1 > cap) {
+    const int64_t c0 = cap * items0 / (items0 + items1);
+    b0 = b0 < c0 ? b0 : (c0 < 1 ? 1 : c0);
+    b1 = b1 < cap - b0 ? b1 : cap - b0;
+  }
+  if (b0 < 1) b0 = 1;
+  const unsigned blocks0 = (unsigned)b0, grid = (unsigned)(b0 + b1);
+  if (in_dtype == CSA_F32) {
+    if (vec == 4)
+      compress_kernel<float, 4><<<grid, 256, 0, st>>>(j0, j1, blocks0, B, T, x_pos0, m, s_begin, n_s);
+    else
+      compress_kernel<float, 1><<<grid, 256, 0, st>>>(j0, j1, blocks0, B, T, x_pos0, m, s_begin, n_s);
+  } else {
+    if (vec == 8)
+      compress_kernel<uint16_t, 8><<<grid, 256, 0, st>>>(j0, j1, blocks0, B, T, x_pos0, m,
+                                                         s_begin, n_s);
+    else
+      compress_kernel<uint16_t, 1><<<grid, 256, 0, st>>>(j0, j1, blocks0, B, T, x_pos0, m,
+                                                         s_begin, n_s);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype, const float* bias,
                             int B, int64_t x_pos0, int64_t T, int m, int C, int64_t s_begin,
                             int64_t s_end, const csa_rows& out, cudaStream_t st) {
@@ -444,40 +550,30 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
           (uint16_t*)out.rope, out.scale, out.n_rows);
     return cudaGetLastError();
   }
-  const int out_mode = out.dtype == CSA_F32 ? 0 : (m <= 16 ? 2 : 1);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  auto grid_for = [&](int vec) {
-    int64_t items = (int64_t)B * n_s * (C / vec);
-    int64_t blocks = ceil_div(items, 256);
-    int64_t cap = (int64_t)sms * 16;
-    return (unsigned)(blocks < cap ? blocks : cap);
-  };
-  // Few entries (a decode step): one channel per thread.  The rare channels
-  // that need the exact-rounding recompute then sit in different threads (a
-  // warp runs its lanes' recomputes one after another), and the grid is wider.
-  const bool few = (int64_t)B * n_s * m < 4096;
-  if (in_dtype == CSA_F32) {
-    if (C % 4 == 0 && !few)
-      compress_kernel<float, 4><<<grid_for(4), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m, C,
-                                                             s_begin, n_s, out.data, out.n_rows,
-                                                             out_mode);
-    else
-      compress_kernel<float, 1><<<grid_for(1), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m, C,
-                                                             s_begin, n_s, out.data, out.n_rows,
-                                                             out_mode);
-  } else {
-    if (C % 8 == 0 && !few)
-      compress_kernel<uint16_t, 8><<<grid_for(8), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m,
-                                                                C, s_begin, n_s, out.data,
-                                                                out.n_rows, out_mode);
-    else
-      compress_kernel<uint16_t, 1><<<grid_for(1), 256, 0, st>>>(x, gate, bias, B, T, x_pos0, m,
-                                                                C, s_begin, n_s, out.data,
-                                                                out.n_rows, out_mode);
+  CJob j0{x, gate, bias, C, out.data, out.n_rows, out.dtype == CSA_F32 ? 0 : (m <= 16 ? 2 : 1)};
+  CJob j1{nullptr, nullptr, nullptr, 0, nullptr, 0, 0};
+  return launch_pool(j0, j1, in_dtype, B, x_pos0, T, m, s_begin, n_s, st);
+}
+
+cudaError_t launch_compress_pair(const void* x0, const void* g0, const float* bias0, int C0,
+                                 const csa_rows& out0, const void* x1, const void* g1,
+                                 const float* bias1, int C1, const csa_rows& out1,
+                                 csa_dtype in_dtype, int B, int64_t x_pos0, int64_t T, int m,
+                                 int64_t s_begin, int64_t s_end, cudaStream_t st) {
+  const int64_t n_s = s_end - s_begin;
+  const bool pair = out0.dtype != CSA_E4M3 && out1.dtype != CSA_E4M3 &&
+                    pool_vec(in_dtype, C0, B, n_s, m) == pool_vec(in_dtype, C1, B, n_s, m);
+  if (n_s <= 0 || B <= 0) return cudaSuccess;
+  if (!pair) {
+    cudaError_t e = launch_compress(x0, g0, in_dtype, bias0, B, x_pos0, T, m, C0, s_begin, s_end,
+                                    out0, st);
+    if (e != cudaSuccess) return e;
+    return launch_compress(x1, g1, in_dtype, bias1, B, x_pos0, T, m, C1, s_begin, s_end, out1, st);
   }
-  return cudaGetLastError();
+  const int mode_bf16 = m <= 16 ? 2 : 1;
+  CJob j0{x0, g0, bias0, C0, out0.data, out0.n_rows, out0.dtype == CSA_F32 ? 0 : mode_bf16};
+  CJob j1{x1, g1, bias1, C1, out1.data, out1.n_rows, out1.dtype == CSA_F32 ? 0 : mode_bf16};
+  return launch_pool(j0, j1, in_dtype, B, x_pos0, T, m, s_begin, n_s, st);
 }
 
 }  // namespace csa

@@ -159,12 +159,12 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float* __restr
 //              row, in index order (ballots), into a list of the (key, index)
 //              composites of its keys >= tau;
 //   C  final:  one CTA per row; if at least kk keys reached tau the kk largest
-//              of the row are all among them: an exact radix select on the
-//              64-bit composite (key << 32 | ~index), whose values are all
-//              distinct and order ties by lower index, gives the threshold, and
-//              the composites at or above it, already in index order, are the
-//              output.  If fewer reached tau (a sample far from the row, never
-//              seen on these workloads), the CTA selects over the whole row.
+//              of the row are all among them: a radix select on their keys
+//              gives the key T of the kk-th largest and how many keys equal to
+//              T are needed, and one pass over the candidates (already in
+//              index order) keeps every key > T and the lowest-index keys == T.
+//              If fewer reached tau (a sample far from the row, never seen on
+//              these workloads), the CTA selects over the whole row.
 // A histogram of the raw key bits would do the same in one pass, but scores
 // often share a few binades, so its atomics pile up on a handful of bins.
 constexpr int kMaxK = 4096;         // largest k of this path
@@ -173,7 +173,7 @@ constexpr int kCandSmem = 8192;     // candidates kernel C keeps in shared memor
 constexpr int kWarpsB = 16;         // warps of kernel B (512 threads)
 constexpr int kMaxSlices = 256;     // slices x kWarpsB lists fit kernel C's shared memory
 constexpr int kMaxLists = kMaxSlices * kWarpsB;
-constexpr int kTargetCtas = 592;    // slices of all rows together (4 x 148), device independent
+constexpr int kTargetCtas = 592;    // slices of all rows together: one wave of 4 x 148 CTAs
 
 struct LongRows {
   int S;                     // slices per row
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(1024) topk_sample_kernel(const float* __restri
   if (threadIdx.x == 0) lr.tau[row] = tau;
 }
 
-__global__ void __launch_bounds__(512) topk_filter_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(512, 4) topk_filter_kernel(const float* __restrict__ scores,
                                                           int64_t q_pos0, int Q, int64_t N, int m,
                                                           int k, LongRows lr) {
   const int64_t row = blockIdx.y;
@@ -278,24 +278,26 @@ __global__ void __launch_bounds__(512) topk_filter_kernel(const float* __restric
   part_range(s1 - s0, kWarpsB, warp, &w0, &w1);
   w0 += s0;
   w1 += s0;
-  const float* srow = scores + row * N;
+  // positions within the row fit 32 bits (rows are < 2^31 entries)
+  const float* wrow = scores + row * N + w0;
   unsigned long long* cand = lr.cand + row * N + w0;
+  const int len = (int)(w1 - w0), pos0 = (int)w0;
   const unsigned lt_mask = (1u << lane) - 1u;
   int nc = 0;
-  for (int64_t base = w0; base < w1; base += 8 * 32) {
+  for (int base = 0; base < len; base += 8 * 32) {
     uint32_t key[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int64_t t = base + j * 32 + lane;
-      key[j] = t < w1 ? score_key(__ldg(srow + t)) : 0u;
+      const int t = base + j * 32 + lane;
+      key[j] = t < len ? score_key(__ldg(wrow + t)) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int64_t t = base + j * 32 + lane;
-      const unsigned b = __ballot_sync(0xffffffffu, t < w1 && key[j] >= tau);
+      const int t = base + j * 32 + lane;
+      const unsigned b = __ballot_sync(0xffffffffu, t < len && key[j] >= tau);
       if ((b >> lane) & 1u)
         cand[nc + __popc(b & lt_mask)] =
-            ((unsigned long long)key[j] << 32) | (unsigned long long)(~(uint32_t)t);
+            ((unsigned long long)key[j] << 32) | (unsigned long long)(~(uint32_t)(pos0 + t));
       nc += __popc(b);
     }
   }
@@ -401,23 +403,27 @@ __global__ void __launch_bounds__(1024) topk_final_kernel(const float* __restric
   if (in_smem)
     for (int f = threadIdx.x; f < nc; f += blockDim.x) cbuf[f] = cand_at(f);
   __syncthreads();
-  unsigned long long thr;
-  if (in_smem)
-    thr = radix_select<unsigned long long, 64>([&](int64_t i) { return cbuf[i]; }, nc, kk, hist,
-                                               &sh_prefix64, &sh_need);
-  else
-    thr = radix_select<unsigned long long, 64>(cand_at, nc, kk, hist, &sh_prefix64, &sh_need);
-  // the composites at or above thr are the kk kept entries, already in index order
-  int taken = 0;
+  // the key of the kk-th largest candidate, and how many keys equal to it
+  // are needed: the lowest-index ones (candidates are in index order)
+  const uint32_t T = radix_select<uint32_t, 32>(
+      [&](int64_t i) { return (uint32_t)((in_smem ? cbuf[i] : cand_at(i)) >> 32); }, nc, kk, hist,
+      &sh_prefix32, &sh_need);
+  const int need_eq = sh_need;
+  int taken = 0, eq_seen = 0;
   for (int base = 0; base < nc; base += blockDim.x) {
     const int f = base + threadIdx.x;
     unsigned long long x = 0;
     if (f < nc) x = in_smem ? cbuf[f] : cand_at(f);
-    const bool take = f < nc && x >= thr;
-    int tot;
-    const int pre = BlockScan::run(take ? 1 : 0, warp_sums, &tot);
-    if (take) orow[taken + pre] = (int32_t)(~(uint32_t)(x & 0xffffffffull));
-    taken += tot;
+    const uint32_t kx = (uint32_t)(x >> 32);
+    const int gt = (f < nc && kx > T) ? 1 : 0;
+    const int eq = (f < nc && kx == T) ? 1 : 0;
+    int eq_tot, take_tot;
+    const int eq_rank = eq_seen + BlockScan::run(eq, warp_sums, &eq_tot);
+    const int take = gt | (eq & (eq_rank < need_eq ? 1 : 0));
+    const int pos = taken + BlockScan::run(take, warp_sums, &take_tot);
+    if (take) orow[pos] = (int32_t)(~(uint32_t)(x & 0xffffffffull));
+    taken += take_tot;
+    eq_seen += eq_tot;
   }
 }
 
@@ -428,7 +434,7 @@ bool use_long_rows(const csa_params& p, int Q, int64_t N) {
 
 int long_rows_slices(const csa_params& p, int Q, int64_t N) {
   const int64_t rows = (int64_t)p.B * Q;
-  int64_t S = ceil_div(kTargetCtas, rows);
+  int64_t S = kTargetCtas / rows;  // no second, partial wave
   const int64_t cap = ceil_div(N, 2048);
   if (S > cap) S = cap;
   if (S > kMaxSlices) S = kMaxSlices;

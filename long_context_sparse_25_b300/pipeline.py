@@ -76,7 +76,7 @@ class Step:
 
     def launches_per_step(self) -> int:
         """Kernels one run() launches, following the library's launch plan:
-        compress (one per cache), the indexer, top-k (three kernels for a few
+        compress (both caches in one launch unless one is e4m3), the indexer, top-k (three kernels for a few
         long rows, one otherwise), attention (the tensor-core kernel for bf16 /
         mixed caches with 128 heads, plus a combine kernel when a decode query
         is split; the CUDA-core kernel plus a combine when its rows are split)."""
@@ -95,7 +95,22 @@ class Step:
         if wl.mode.startswith("hca"):
             return 1 + attend
         topk = 3 if (wl.N > 16384 and wl.k <= 4096 and rows < 256) else 1
-        return 2 + 1 + topk + attend
+        return self._compress_launches() + 1 + topk + attend
+
+    def _compress_launches(self) -> int:
+        """csa_forward pools the new blocks into both caches with one launch when
+        neither cache is e4m3 and both take the same channels-per-thread width
+        (16-byte loads, or one channel per thread for a step of few blocks)."""
+        wl = self.wl
+        n_s = wl.N - self.n_cached
+        if n_s <= 0:
+            return 0
+        if wl.dtype == "mixed":
+            return 2
+        few = wl.B * n_s * wl.m < 4096
+        per = 4 if wl.dtype == "f32" else 8
+        vec = [1 if (few or c % per) else per for c in (wl.D_qk, wl.d_I)]
+        return 1 if vec[0] == vec[1] else 2
 
     def run(self, stream=None):
         wl = self.wl
