@@ -340,25 +340,58 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
 
     per_part = {name: timed(g_, args.steps) / args.steps for name, g_ in g_part.items()}
 
-    # end to end: the step's new inputs from pinned host memory, the output back
-    h2d = [inp[k] for k in ("q", "q_idx", "w", "x", "g", "xi", "gi") if k in inp]
-    if "q_idx_scale" in inp:
-        h2d.append(inp["q_idx_scale"])
-    host_in = [t_.cpu().pin_memory() for t_ in h2d]
-    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    bi = sum(t_.numel() * t_.element_size() for t_ in h2d)
-    bo = host_out.numel() * host_out.element_size()
+    # end to end: every step copies its new inputs from pinned host memory and
+    # its output back.  Two sets of per-step buffers (the caches are shared)
+    # with a graph each let step i+1's input copies and step i-1's output copy
+    # run while step i computes: host->device on one stream, device->host on
+    # another, the step on the compute stream, ordered by events.
+    keys_in = [k for k in ("q", "q_idx", "w", "x", "g", "xi", "gi", "q_idx_scale") if k in inp]
+    inp2 = dict(inp)
+    for k in keys_in:
+        inp2[k] = inp[k].clone()
+    step2 = Step(wl, inp2)
+    g_full2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full2, stream=stream):
+        step2.run(stream=stream)
+    sets = [(step, g_full, [inp[k] for k in keys_in]), (step2, g_full2, [inp2[k] for k in keys_in])]
+    host_in = [inp[k].cpu().pin_memory() for k in keys_in]
+    host_out = [torch.empty(st_.out.shape, dtype=st_.out.dtype, pin_memory=True) for st_, _, _ in sets]
+    bi = sum(t_.numel() * t_.element_size() for t_ in host_in)
+    bo = host_out[0].numel() * host_out[0].element_size()
     ne = e2e_steps or args.steps
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    in_done, step_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for it in range(ne + 2):
-            if it == 2:
-                e0.record(stream)
-            for d_, h_ in zip(h2d, host_in):
-                d_.copy_(h_, non_blocking=True)
-            g_full.replay()
-            host_out.copy_(step.out, non_blocking=True)
-        e1.record(stream)
+
+    def e2e_steps_run(n, first):
+        for it in range(n):
+            k = it % 2
+            st_, g_, dev_in = sets[k]
+            if it >= 2 or not first:
+                h2d_s.wait_event(step_done[k])  # the step that last read set k is done
+            with torch.cuda.stream(h2d_s):
+                for d_, h_ in zip(dev_in, host_in):
+                    d_.copy_(h_, non_blocking=True)
+                in_done[k].record(h2d_s)
+            stream.wait_event(in_done[k])
+            if it >= 2 or not first:
+                stream.wait_event(out_done[k])  # set k's output has been read back
+            with torch.cuda.stream(stream):
+                g_.replay()
+                step_done[k].record(stream)
+            d2h_s.wait_event(step_done[k])
+            with torch.cuda.stream(d2h_s):
+                host_out[k].copy_(st_.out, non_blocking=True)
+                out_done[k].record(d2h_s)
+
+    e2e_steps_run(2, True)  # warm-up
+    torch.cuda.synchronize()
+    e0.record(h2d_s)
+    e2e_steps_run(ne, False)
+    stream.wait_stream(d2h_s)
+    stream.wait_stream(h2d_s)
+    e1.record(stream)
     torch.cuda.synchronize()
     te = torch.tensor([e0.elapsed_time(e1) / ne], dtype=torch.float64, device=dev)
     if dist:
@@ -369,7 +402,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
            "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
            "launches_per_step": step.launches_per_step()}
-    del step, inp, g_full, g_part, host_in, host_out
+    del step, step2, inp, inp2, g_full, g_full2, g_part, host_in, host_out
     gc.collect()
     torch.cuda.empty_cache()
     return res

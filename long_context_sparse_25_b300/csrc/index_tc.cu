@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       const uint32_t b_chunk16 = a.b_chunk_bytes >> 4;
       uint32_t s = 0, s_ph = 0;      // ring stage and the parity of its fill
       uint32_t acc = 0, acc_ph = 0;  // accumulator buffer and its parity
+      bool a_ready = false, acc_ready = false;  // already seen by an early probe
       uint32_t qcount = 0, bi = 0;
       int pb = -1, pqb = -1;
       bool ok = true;
@@ -250,8 +251,17 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
           pb = b;
           pqb = qb;
         }
-        if (!tc::mbar_wait(&a_full[s], s_ph, err, 4)) { ok = false; break; }
-        if (!tc::mbar_wait(&acc_empty[acc], acc_ph ^ 1, err, 5)) { ok = false; break; }
+        if (!a_ready && !tc::mbar_wait(&a_full[s], s_ph, err, 4)) { ok = false; break; }
+        if (!acc_ready && !tc::mbar_wait(&acc_empty[acc], acc_ph ^ 1, err, 5)) { ok = false; break; }
+        // probe the next stage's fill and the next accumulator's release now
+        // (non-blocking): each answer is needed only at the next tile, so the
+        // latency of the probes overlaps this tile's MMA issue
+        {
+          const uint32_t ns = s + 1 == (uint32_t)a.stages ? 0 : s + 1;
+          const uint32_t na = acc + 1 == (uint32_t)a.nacc ? 0 : acc + 1;
+          a_ready = tc::mbar_test_wait(&a_full[ns], ns == 0 ? s_ph ^ 1 : s_ph);
+          acc_ready = tc::mbar_test_wait(&acc_empty[na], (na == 0 ? acc_ph ^ 1 : acc_ph) ^ 1);
+        }
         tc::tc_fence_after();
         const uint32_t d = tmem_base + acc * NM;
         const uint64_t ad = ad0 + s * a_stage16, bd = bd0 + bi * b_buf16;
