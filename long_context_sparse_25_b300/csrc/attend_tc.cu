@@ -54,6 +54,8 @@
 // timeout is recorded in a device error word and the kernel returns.
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -258,7 +260,9 @@ __device__ __forceinline__ void cp_async_wait() {
 
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const AttArgs a) {
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_raw, const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -314,6 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(mma_done, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tm_q);
+    if (!kE4M3) {
+      tc::prefetch_tmap(&tm_kv);
+      if (a.W > 0) tc::prefetch_tmap(&tm_raw);
+    }
 
   }
   if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, 512);
@@ -360,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sp[kUnits];
         uint32_t wb;
         SlotSrc s0, s1;
+        int tma;    // bf16 caches: 1 = 128 consecutive entry rows, 2 = 128 consecutive
+        int tma_y;  //   raw rows (from tma_y), loaded by one TMA box per chunk; 0 = gathered
       };
       auto issue_chunk = [&](int c, int mode, const TileRows& t) -> bool {
         int okw = 1;
@@ -367,7 +377,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) return false;
         const uint32_t dst = tc::smem_u32(sRing + pslot * kChunk);
-        if (kE4M3) {
+        if (!kE4M3 && t.tma) {
+          // one TMA box: the chunk's barrier completes on its bytes and on the
+          // producers' arrivals (one of them carries the byte count)
+          if (pt == 0) {
+            tc::mbar_expect_tx(&ring_full[pslot], kChunk);
+            tc::tma_load_2d(sRing + pslot * kChunk, t.tma == 1 ? &tm_kv : &tm_raw,
+                            &ring_full[pslot], c * 64, t.tma_y);
+          } else {
+            tc::mbar_arrive(&ring_full[pslot]);
+          }
+        } else if (kE4M3) {
           // every load of the chunk in flight first, then the conversions
           RawUnit raw[kUnits];
 #pragma unroll
@@ -426,6 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           t.rr[i] = ss.row;
           t.wb |= (ss.win ? 1u : 0u) << i;
           t.sp[i] = (ss.win ? rawb : kvb) + ss.row * rowb + (unit & 7) * 16;
+        }
+        t.tma = 0;
+        t.tma_y = 0;
+        if (!kE4M3) {
+          if (a.dense && jt + kT <= kl.kd) {
+            // every slot a valid entry, entry j in row j (a tile with masked
+            // slots is gathered: rows past the valid entries may hold anything,
+            // and a masked slot's row still meets a zero weight in P . V)
+            t.tma = 1;
+            t.tma_y = (int)((int64_t)b * a.kv_rows + jt);
+          } else if (a.W > 0 && jt >= kl.k_ent) {
+            // every slot a window slot: raw rows lo + (j - k_ent) (past the
+            // window: masked; past the cache: zero-filled)
+            t.tma = 2;
+            t.tma_y = (int)((int64_t)b * a.raw_rows + (kl.lo - a.raw_pos0) + (jt - kl.k_ent));
+          }
         }
         t.s0 = slot_src(a, kl, b, jt + pt, tw.w[kUnits]);
         t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[kUnits + 1]);
@@ -923,8 +959,18 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
                                   ((rows * p.D_v * sizeof(float) + 255) & ~(size_t)255));
 
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_kv, tm_raw;
+  memset(&tm_kv, 0, sizeof(tm_kv));
+  memset(&tm_raw, 0, sizeof(tm_raw));
   if (!make_map_bf16(&tm_q, q, (int64_t)p.B * Q * p.H, p.D_qk, 128)) return cudaErrorInvalidValue;
+  // bf16 caches: dense runs of entry rows and window rows load as 128-row boxes
+  if (!a.e4m3) {
+    if (!make_map_bf16(&tm_kv, kv.data, (int64_t)p.B * kv.n_rows, p.D_qk, 128))
+      return cudaErrorInvalidValue;
+    if (p.window > 0 &&
+        !make_map_bf16(&tm_raw, raw.data, (int64_t)p.B * raw.n_rows, p.D_qk, 128))
+      return cudaErrorInvalidValue;
+  }
   const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
@@ -934,12 +980,12 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, a);
+    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
   } else {
     e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, a);
+    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
