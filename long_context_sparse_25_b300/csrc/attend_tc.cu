@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + (size_t)kRing * kChunk);
   uint64_t* ring_full = bars;
   uint64_t* ring_empty = bars + kRing;
-  uint64_t* q_full = bars + 2 * kRing;
-  uint64_t* s_full = q_full + 1;      // [2]
+  uint64_t* q_full = bars + 2 * kRing;  // [kMaxQChunks]: one per Q chunk
+  uint64_t* s_full = q_full + kMaxQChunks;  // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* mask_full = p_full + 2;   // [2]
   uint64_t* mask_empty = mask_full + 2;  // [2]
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&ring_full[s], kProdWarps * 32);  // every producer thread arrives
       tc::mbar_init(&ring_empty[s], 1);
     }
-    tc::mbar_init(q_full, 1);
+    for (int c = 0; c < kMaxQChunks; ++c) tc::mbar_init(&q_full[c], 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&s_full[s], 1);
       tc::mbar_init(&p_full[s], 4);
@@ -342,9 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pt = threadIdx.x;
     if (n > 0) {
       if (pt == 0) {
-        tc::mbar_expect_tx(q_full, a.nc * kChunk);
-        for (int c = 0; c < a.nc; ++c)
-          tc::tma_load_2d(sQ + c * kChunk, &tm_q, q_full, c * 64, (int)(qrow * a.H));
+        // a barrier per chunk: the first tile's QK^T starts as its Q chunks land
+        for (int c = 0; c < a.nc; ++c) {
+          tc::mbar_expect_tx(&q_full[c], kChunk);
+          tc::tma_load_2d(sQ + c * kChunk, &tm_q, &q_full[c], c * 64, (int)(qrow * a.H));
+        }
       }
       const uint8_t* kvb = reinterpret_cast<const uint8_t*>(a.kv16);
       const uint8_t* rawb = reinterpret_cast<const uint8_t*>(a.raw16);
@@ -418,34 +420,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      // key-list words of a tile's slots for this thread (units, then the two
-      // mask slots), fetched ahead of tile_rows
+      // A warp's units of a chunk cover 44 key rows (unit i of lane L is row
+      // 4 warp + 12 i + L/8, shared by 8 lanes): lane L looks up rows q = L
+      // and q = L + 32 of that list and the lanes exchange them by shuffles.
+      // Key-list words are fetched a tile ahead: those two rows, then the two
+      // mask slots pt and pt + 96.
       struct TileWords {
-        int32_t w[kUnits + 2];
+        int32_t w[4];
       };
       const bool has1 = pt + kProd < kT;
+      auto unit_row = [&](int q) -> int { return 4 * warp + 12 * (q >> 2) + (q & 3); };
+      const int q1 = lane, q2 = lane + 32;
+      const bool has_q2 = q2 < 4 * kUnits;
       auto tile_words = [&](int u, TileWords& t) {
         const int jt = (tile0 + u) * kT;
-#pragma unroll
-        for (int i = 0; i < kUnits; ++i) {
-          const int unit = pt + kProd * i;
-          const int r = unit < (int)(kChunk / 16) ? unit >> 3 : 0;
-          t.w[i] = slot_word(a, kl, qrow, jt + r);
-        }
-        t.w[kUnits] = slot_word(a, kl, qrow, jt + pt);
-        t.w[kUnits + 1] = slot_word(a, kl, qrow, jt + (has1 ? pt + kProd : pt));
+        const int r1 = unit_row(q1), r2 = unit_row(q2);
+        t.w[0] = r1 < kT ? slot_word(a, kl, qrow, jt + r1) : 0;
+        t.w[1] = (has_q2 && r2 < kT) ? slot_word(a, kl, qrow, jt + r2) : 0;
+        t.w[2] = slot_word(a, kl, qrow, jt + pt);
+        t.w[3] = slot_word(a, kl, qrow, jt + (has1 ? pt + kProd : pt));
       };
       auto tile_rows = [&](int u, const TileWords& tw, TileRows& t) {
         const int jt = (tile0 + u) * kT;
+        // (row | win << 63) of this lane's two rows of the warp's list
+        auto packed = [&](int r, int32_t word) -> unsigned long long {
+          const SlotSrc ss = slot_src(a, kl, b, jt + (r < kT ? r : 0), word);
+          return (unsigned long long)ss.row | ((unsigned long long)(ss.win ? 1 : 0) << 63);
+        };
+        const unsigned long long v1 = packed(unit_row(q1), tw.w[0]);
+        const unsigned long long v2 = has_q2 ? packed(unit_row(q2), tw.w[1]) : 0ull;
         t.wb = 0;
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
-          const int unit = pt + kProd * i;
-          const int r = unit < (int)(kChunk / 16) ? unit >> 3 : 0;
-          const SlotSrc ss = slot_src(a, kl, b, jt + r, tw.w[i]);
-          t.rr[i] = ss.row;
-          t.wb |= (ss.win ? 1u : 0u) << i;
-          t.sp[i] = (ss.win ? rawb : kvb) + ss.row * rowb + (unit & 7) * 16;
+          const int src = 4 * i + (lane >> 3);
+          const unsigned long long a1 = __shfl_sync(0xffffffffu, v1, src & 31);
+          const unsigned long long a2 = __shfl_sync(0xffffffffu, v2, src & 31);
+          const unsigned long long v = src < 32 ? a1 : a2;
+          const int64_t row = (int64_t)(v & ~(1ull << 63));
+          const bool win = (v >> 63) != 0;
+          t.rr[i] = row;
+          t.wb |= (win ? 1u : 0u) << i;
+          t.sp[i] = (win ? rawb : kvb) + row * rowb + (lane & 7) * 16;
         }
         t.tma = 0;
         t.tma_y = 0;
@@ -463,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             t.tma_y = (int)((int64_t)b * a.raw_rows + (kl.lo - a.raw_pos0) + (jt - kl.k_ent));
           }
         }
-        t.s0 = slot_src(a, kl, b, jt + pt, tw.w[kUnits]);
-        t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[kUnits + 1]);
+        t.s0 = slot_src(a, kl, b, jt + pt, tw.w[2]);
+        t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[3]);
       };
       TileRows cur, prev;
       TileWords wnext;
@@ -506,14 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every copy must land before the CTA can exit (their arrivals on the
       // ring barriers happen by themselves)
       cp_async_wait<0>();
-      if (pt == 0) tc::mbar_drain(q_full, 0);
+      if (pt == 0)
+        for (int c = 0; c < a.nc; ++c) tc::mbar_drain(&q_full[c], 0);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       const uint32_t id_s = tc::idesc(128, kT, 1, 1);
       const uint32_t id_pv = tc::idesc(128, 64, 1, 1, 0, 1);
-      bool ok = tc::mbar_wait(q_full, 0, err, 21);
+      bool ok = true;
+      uint32_t q_seen = 0;  // Q chunks known to have landed
       // descriptors of Q chunk 0 and ring slot 0 (K-major for S, MN-major
       // for PV); other chunks / slots / K steps are constant offsets in the
       // start-address field, so each MMA costs the issuing thread a couple of
@@ -560,6 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_tmem = tmem + sb * 128;
         for (int cc = 0; cc < a.nsc && ok; ++cc) {
           const int c = cc < a.nc ? cc : cc - a.nc;  // the Q chunk this key chunk meets
+          if (!((q_seen >> c) & 1u)) {
+            if (!tc::mbar_wait(&q_full[c], 0, err, 21)) { ok = false; break; }
+            q_seen |= 1u << c;
+          }
           if (!tc::mbar_wait(&ring_full[slot], ph, err, 24)) { ok = false; break; }
           if (!kE4M3) tc::fence_proxy_async_smem();  // cp.async rows -> tensor cores
           tc::tc_fence_after();
@@ -974,7 +995,7 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
-                      (2 * kRing + 13) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
+                      (2 * kRing + 12 + kMaxQChunks) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
   cudaError_t e;
   if (a.e4m3) {
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
