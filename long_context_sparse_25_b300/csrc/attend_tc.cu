@@ -244,6 +244,30 @@ __device__ __forceinline__ uint4 manual_convert(const RawUnit& r, int mode) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Both parts of a unit for QK^T from one load: the kHi conversion and the
+// kLo conversion of the same unit (kind 0 / 2 rows: the values, zeros).
+__device__ __forceinline__ void manual_convert_pair(const RawUnit& r, uint4& hi, uint4& lo) {
+  if (r.kind != 1) {
+    hi = r.v;
+    lo = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint32_t w2[2] = {r.v.x, r.v.y};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t word = w2[e / 2];
+    const int sh = (e & 1) * 16;
+    const float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * r.sc;
+    const float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * r.sc;
+    h[e] = pack_bf16(f0, f1);
+    l[e] = pack_bf16(f0 - __bfloat162float(__float2bfloat16_rn(f0)),
+                     f1 - __bfloat162float(__float2bfloat16_rn(f1)));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -420,6 +444,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      // Mixed caches: the high and the low part of nope chunk c go to two
+      // consecutive slots from one load and one dequantisation.
+      auto issue_pair = [&](int c, const TileRows& t) -> bool {
+        const uint32_t s0 = pslot, p0 = pph;
+        const uint32_t s1 = pslot + 1 == kRing ? 0 : pslot + 1;
+        const uint32_t p1 = s1 == 0 ? pph ^ 1 : pph;
+        int okw = 1;
+        if (lane == 0)
+          okw = tc::mbar_wait(&ring_empty[s0], p0 ^ 1, err, 11) &&
+                tc::mbar_wait(&ring_empty[s1], p1 ^ 1, err, 11);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) return false;
+        RawUnit raw[kUnits];
+#pragma unroll
+        for (int i = 0; i < kUnits; ++i) {
+          const int unit = pt + kProd * i;
+          if (unit < (int)(kChunk / 16))
+            raw[i] = manual_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7, kHi);
+        }
+#pragma unroll
+        for (int i = 0; i < kUnits; ++i) {
+          const int unit = pt + kProd * i;
+          if (unit < (int)(kChunk / 16)) {
+            uint4 hi, lo;
+            manual_convert_pair(raw[i], hi, lo);
+            *reinterpret_cast<uint4*>(sRing + s0 * kChunk + dso[i]) = hi;
+            *reinterpret_cast<uint4*>(sRing + s1 * kChunk + dso[i]) = lo;
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&ring_full[s0]);
+        tc::mbar_arrive(&ring_full[s1]);
+        pslot = s1 + 1 == kRing ? 0 : s1 + 1;
+        pph = pslot == 0 ? p1 ^ 1 : p1;
+        return true;
+      };
       // A warp's units of a chunk cover 44 key rows (unit i of lane L is row
       // 4 warp + 12 i + L/8, shared by 8 lanes): lane L looks up rows q = L
       // and q = L + 32 of that list and the lanes exchange them by shuffles.
@@ -510,8 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
-          for (int cc = 0; cc < a.nsc && ok; ++cc)
-            ok = cc < a.nc ? issue_chunk(cc, kHi, cur) : issue_chunk(cc - a.nc, kLo, cur);
+          // QK^T chunks: mixed caches first the (high, low) pairs of the nope
+          // chunks, then the RoPE chunks; bf16 caches the nc chunks in order
+          const int nlo = kE4M3 ? a.nsc - a.nc : 0;
+          if (kE4M3)
+            for (int c = 0; c < nlo && ok; ++c) ok = issue_pair(c, cur);
+          for (int c = nlo; c < a.nc && ok; ++c) ok = issue_chunk(c, kHi, cur);
         }
         if (u >= 1)
           for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev);
@@ -576,7 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = u & 1;
         const uint32_t s_tmem = tmem + sb * 128;
         for (int cc = 0; cc < a.nsc && ok; ++cc) {
-          const int c = cc < a.nc ? cc : cc - a.nc;  // the Q chunk this key chunk meets
+          // the Q chunk this key chunk meets (the producers' order: mixed
+          // caches' (high, low) pairs of the nope chunks, then the rest)
+          const int nlo = kE4M3 ? a.nsc - a.nc : 0;
+          const int c = cc < 2 * nlo ? cc >> 1 : cc - nlo;
           if (!((q_seen >> c) & 1u)) {
             if (!tc::mbar_wait(&q_full[c], 0, err, 21)) { ok = false; break; }
             q_seen |= 1u << c;
