@@ -1,9 +1,10 @@
-"""Parity at the full size of the timed workload: CSA decode at 1M-token
-context, B = 32 (262,144 entries per sequence), in the launch configuration
-bench.py times (one csa_forward per step).  Every sequence: the compressed
-tail entry and key bit-exact, every visible score within 1e-5 of the row
-scale, the selection within the swap rule; the attention output on a fixed
-sample of 8 sequences (the oracle evaluates the 1152 keys each query keeps)."""
+"""Parity at the full size of the timed workloads, in the launch configuration
+bench.py times.  CSA decode at 1M-token context, B = 32 (262,144 entries per
+sequence, one csa_forward per step): every sequence's compressed tail entry
+and key bit-exact, every visible score within 1e-5 of the row scale, the
+selection within the swap rule; the attention output on a fixed sample of 8
+sequences (the oracle evaluates the 1152 keys each query keeps).  CSA prefill
+at 64K tokens and HCA prefill at 1M tokens on fixed query samples."""
 
 import numpy as np
 import pytest
@@ -105,3 +106,44 @@ def test_prefill_64k_full_size(cuda_device):
     check_selection(sel, ref, O.n_vis(pos, m), wl.k)
     o = O.csa_attend(f64(inp["q"][0][tq]), kv, x, wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)
     check_out(f64(step.out[0][tq]), o, False)
+
+
+def test_hca_prefill_1m_full_size(cuda_device):
+    """HCA prefill at 2^20 tokens (8,192 entries of m' = 128 raw rows, the
+    last 8,192 queries, 128 heads), in the launch configuration bench.py
+    times (csa_compress, then hca_attend): every compressed entry within one
+    bf16 ulp of the oracle's (fp32 pooling rounded once), and the attention
+    output of a fixed query sample (the first 4, 8 spread over the rest, the
+    last 4).  Late queries see all 8,192 entries, 64 full tiles of
+    consecutive entry rows."""
+    wl = synth.WORKLOADS["hca_prefill_1m"]
+    dev = cuda_device
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    csa.device_status()  # no bounded device-side wait gave up
+    m, N = wl.m, wl.N
+    got = f64(step.kv_buf[0])
+    ents = np.empty_like(got)
+    bias = f64(inp["bias"])
+    per = 512  # entries per oracle call (bounded host memory)
+    for e0 in range(0, N, per):
+        e1 = min(N, e0 + per)
+        a, b_ = e0 * m - wl.raw_pos0, e1 * m - wl.raw_pos0
+        ents[e0:e1] = O.compress(f64(inp["x"][0][a:b_]), f64(inp["g"][0][a:b_]), bias, m)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ents), 1e-30))) - 7)
+    assert np.all(np.abs(got - ents) <= ulp + 1e-6), "HCA entries off by more than 1 ulp"
+    stored = O.store_rows(ents, "bf16")
+    qs = np.unique(np.concatenate([np.arange(4), np.linspace(0, wl.Q - 1, 8).astype(int),
+                                   np.arange(wl.Q - 4, wl.Q)]))
+    tq = torch.from_numpy(qs).to(dev).long()
+    q = f64(inp["q"][0][tq])
+    ref = np.empty((qs.size, wl.H, wl.D_v))
+    for j, i in enumerate(qs):
+        t = wl.q_pos0 + int(i)
+        lo, hi = O.window_range(t, wl.W)
+        raw = f64(inp["x"][0][lo - wl.raw_pos0: hi - wl.raw_pos0])  # the query's window rows
+        ref[j] = O.hca_attend(q[j:j + 1], stored, raw, lo, np.array([t]), m, wl.W, wl.D_v,
+                              wl.scale)[0]
+    check_out(f64(step.out[0][tq]), ref, False)
