@@ -56,6 +56,20 @@ def _peaks():
     return dict(FALLBACK), "fallback"
 
 
+def max_over_ranks(x: float, dist, dev) -> float:
+    """The largest x of any rank: a job's time is its slowest rank's."""
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_units(wl, world: int) -> int:
+    """Units (tokens) the whole job processes per step: each rank runs its own
+    batch of the workload (replicas, no exchange on the data path)."""
+    return wl.B * wl.Q * world
+
+
 def _blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -332,10 +346,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item()) / args.steps
+    ms = max_over_ranks(total_ms, dist, dev) / args.steps
     csa.device_status(stream)
 
     per_part = {name: timed(g_, args.steps) / args.steps for name, g_ in g_part.items()}
@@ -393,11 +404,8 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     stream.wait_stream(h2d_s)
     e1.record(stream)
     torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1) / ne], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
-    units = wl.B * wl.Q * world
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne, dist, dev)
+    units = job_units(wl, world)
     res = {"ms": ms, "value": units / (ms / 1e3), "per_part_ms": per_part, "clocks": clk,
            "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
