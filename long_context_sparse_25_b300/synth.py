@@ -72,9 +72,10 @@ class Workload:
 
     @property
     def raw_rows(self) -> int:
-        """Raw rows held in memory: all L for prefill, the window (which also
-        covers the block completed by the decode token) for decode."""
-        return self.L if self.mode.endswith("prefill") else max(self.W, self.m)
+        """Raw rows held in memory: all L for prefill; for decode the windows of
+        the step's Q queries (W + Q - 1 rows), which also cover the block the
+        last token completes."""
+        return self.L if self.mode.endswith("prefill") else max(self.W + self.Q - 1, self.m)
 
     @property
     def raw_pos0(self) -> int:

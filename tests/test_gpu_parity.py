@@ -27,6 +27,9 @@ CSA_CASES = {
     "decode_bf16": (W["csa_decode_1m"].replace(B=3, L=20000), None),
     # mixed e4m3 + bf16 decode, 5001 entries
     "decode_mixed": (W["csa_decode_fp8_512k"].replace(B=2, L=20004), None),
+    # a decode step with two new tokens per sequence (the first sees one entry
+    # fewer): the tensor-core indexer's causal schedule with one query per block
+    "decode_bf16_q2": (W["csa_decode_1m"].replace(B=2, L=20000, Q=2), None),
 }
 
 
