@@ -15,14 +15,19 @@
 // (N = 256) so that each key tile read from L2 feeds 4x more MMA work.
 //
 // Roles (warp-specialised, one CTA per SM, persistent):
-//   warp 0      TMA producer: key tiles into a ring of stages, query blocks
-//               into one or two B buffers;
-//   warp 1      TMEM allocator and MMA issuer (one thread);
-//   warps 2..   epilogue: tcgen05.ld of the accumulator, ReLU, weighted head
-//               sum, e4m3 row scales, coalesced fp32 stores of the scores.
-// Accumulators are double-buffered in TMEM so the epilogue of tile t overlaps
-// the MMA of tile t+1.  Every mbarrier wait is bounded; a timeout is recorded
-// in a device error word (read by csa_device_status) and the kernel returns.
+//   warp 0      TMA producer: key tiles into a ring of stages (about 128 KB
+//               in flight), query blocks into one or two B buffers;
+//   warp 1      TMEM allocator and MMA issuer (one thread; descriptors are
+//               advanced by constant offsets in an unrolled K loop, and the
+//               next stage's and accumulator's barriers are probed ahead);
+//   warps 2-9   two epilogue warpgroups: tcgen05.ld of the accumulator, ReLU,
+//               weighted head sum, e4m3 row scales, coalesced fp32 stores of
+//               the scores.  They take alternate tiles (decode) or split the
+//               queries of an N = 256 tile (prefill).
+// Up to eight accumulators live in TMEM, so the MMA of a tile never waits for
+// the epilogue of an earlier one.  Every mbarrier wait is bounded; a timeout
+// is recorded in a device error word (read by csa_device_status) and the
+// kernel returns.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
