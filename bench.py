@@ -436,6 +436,7 @@ def roofline(wl, per_part, peaks, peak_kind):
         peak = peaks["bf16_tflops"]
         return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
                 "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
+                "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "traffic": _traffic(f"{name}:{wl.name}"), "algorithmic_flops_per_launch": w["hca_flops"]}
     if wl.mode == "csa_decode":
         name = "index"
@@ -450,6 +451,7 @@ def roofline(wl, per_part, peaks, peak_kind):
     peak = peaks["bf16_tflops"]
     return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
             "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
+            "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
             "traffic": _traffic(f"{name}:{wl.name}"),
             "algorithmic_flops_per_launch": w[f"{name}_flops"],
             "other_part": {k: (w[f"{k}_flops"] / (per_part[k] / 1e3) / 1e12) / peak
