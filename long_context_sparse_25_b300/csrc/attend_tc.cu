@@ -1,6 +1,7 @@
 // Tensor-core path of steps 4 / 5 (CSA sparse MQA, HCA dense MQA): tcgen05
-// MMAs with TMEM accumulators, keys gathered by TMA into a ring of
-// 128-byte-swizzled shared-memory chunks.
+// MMAs with TMEM accumulators, key rows gathered (cp.async, or one TMA box per
+// chunk for runs of consecutive rows) into a ring of 128-byte-swizzled
+// shared-memory chunks.
 //
 //   o[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . K_j) * K_j[0:D_v]
 //
@@ -21,7 +22,8 @@
 // the same buffer, and P . V runs with A taken from TMEM.
 //
 // Shared memory: Q of the query (D_qk/64 chunks of 128 x 64 bf16, loaded once
-// by TMA and resident) and a ring of kRing chunks of 128 keys x 64 dims.  For
+// by TMA, a barrier per chunk, and resident) and a ring of kRing chunks of 128
+// keys x 64 dims.  For
 // every tile of 128 keys three producer warps gather the D_qk/64 chunks of the
 // keys and then, one tile later, the D_v/128 chunks of the value half, with
 // 16-byte cp.async copies: each lane computes its own gathered row address
@@ -30,10 +32,13 @@
 // copies of a chunk arrive on the chunk's barrier by themselves once they
 // have landed (cp.async.mbarrier.arrive), so the producers run ahead as far
 // as the ring allows; the MMA issuer, after its wait, issues the proxy fence
-// that makes the rows visible to the tensor cores.  Mixed-precision caches (e4m3 codes with a row scale, RoPE dims in
-// bf16) are converted by the producers themselves: for QK^T each dequantised
-// key is split exactly into a bf16 high part and a bf16 low part (two chunk
-// loads per nope chunk, both multiplied by the same Q chunk), so the scores
+// that makes the rows visible to the tensor cores.  A tile whose 128 slots
+// are all valid consecutive entries (HCA) or all window slots is one TMA box
+// per chunk instead.  Mixed-precision caches (e4m3 codes with a row scale,
+// RoPE dims in bf16) are converted by the producers themselves: for QK^T each
+// dequantised key is split exactly into a bf16 high part and a bf16 low part
+// (one load per nope chunk fills two ring slots, both multiplied by the same
+// Q chunk), so the scores
 // see the key to about 2^-17; for PV the chunk holds the codes themselves
 // (exact in bf16) and the row scale is folded into P, which is split the same
 // way (PV runs on the high and on the low part).  The MMA order is S(0),
@@ -50,8 +55,9 @@
 // merges the splits in order in attend_tc_combine_kernel.
 //
 // Roles: warps 0-2 producers, warp 3 TMEM allocator + MMA issuer (one
-// thread), warps 4-7 softmax / rescale / epilogue.  Every mbarrier wait is bounded; a
-// timeout is recorded in a device error word and the kernel returns.
+// thread; descriptors advanced by constant offsets), warps 4-7 softmax /
+// rescale / epilogue.  Every mbarrier wait is bounded; a timeout is recorded
+// in a device error word and the kernel returns.
 #include <cudaTypedefs.h>
 
 #include <cstring>
