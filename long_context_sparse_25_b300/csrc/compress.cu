@@ -9,9 +9,12 @@
 //
 // The work is a pure stream over x and the gates (HBM bound): one thread owns
 // VEC adjacent channels of one entry and reads them with 16-byte loads, so a
-// warp reads whole 512-byte stretches of a row.  The softmax is taken in two
-// passes over the m rows (max, then exp / sums); the second pass re-reads
-// rows the same thread has just read (L1 hits).
+// warp reads whole 512-byte stretches of a row.  For m <= 16 the softmax is
+// taken in two passes over the m rows (max, then exp / sums; the second pass
+// re-reads rows the same thread has just read, L1 hits); blocks of more rows
+// (m' = 128) are read once with a running maximum.  One launch can pool the
+// same blocks into two caches (the KV entries and the indexer keys of a
+// decode step), each cache a contiguous range of CTAs.
 #include "common.cuh"
 
 namespace csa {
