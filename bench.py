@@ -20,6 +20,16 @@ score the 5.4e8 visible (query, entry) pairs, keep the top 1024 per query,
 attend over them plus 128 window tokens.  Its 9.7 GB query tensor and 4.3 GB
 score matrix are far larger than L2.
 
+The line's ``roofline`` describes the part of the step that takes the longest
+(each part timed alone), lists every part's fraction, and gives the step's own
+fraction (all algorithmic bytes or flops of a step over its time).  ``e2e``
+runs the same step with its new inputs copied from pinned host memory every
+step (decode: the new token's query rows and its raw rows; the earlier raw
+rows of the window arrived with earlier steps and stay resident) and the
+output read back, the copies overlapped with the neighbouring steps.  Every
+line carries ``cpu_baseline``: the oracle timed on a bounded sample of the
+same workload on the host cores.
+
 With --gpus N > 1 (torchrun, one process per GPU) every rank runs its own
 batch (replicas, weak scaling; no collective on the data path) and the time
 is the max over ranks.
@@ -38,6 +48,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 from pathlib import Path
 
@@ -46,6 +57,7 @@ import torch
 ROOT = Path(__file__).resolve().parent
 METRIC = "CSA decode tok/s & prefill query-tok/s at 1M ctx; % of HBM/tensor roofline"
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NOMINAL_BF16_TFLOPS = 2250.0  # datasheet dense bf16 of one B300 (context for the fractions)
 
 
 def _peaks():
@@ -82,30 +94,149 @@ def _blas_threads() -> int:
 
 
 # ---------------------------------------------------------------- CPU oracle
-def _oracle_decode_step(wl, inp, b):
-    """The oracle's complete decode step for sequence b (test infrastructure:
-    used here only for the timed CPU baseline)."""
+# The timed CPU baseline: the float64 oracle as it stands, on the host cores,
+# over a bounded sample of each workload (test infrastructure; this leg and
+# --impl reference are the only places bench.py runs it).
+
+def _f64(t):
+    """Exact float64 values of a tensor's elements (fp32 / bf16 / e4m3)."""
     import numpy as np
     import oracle as O
-
-    def f64(t):
-        t = t.contiguous()
-        if t.dtype == torch.float32:
-            return t.double().numpy()
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.double().numpy()
+    if t.dtype == torch.bfloat16:
         return O.decode_bf16(t.view(torch.int16).numpy().view(np.uint16))
+    return O.decode_e4m3(t.view(torch.uint8).numpy())
 
+
+def _seq_inputs(wl, inp, b):
+    """One sequence's inputs of a decode step as float64 arrays (caches
+    dequantised exactly)."""
+    d = {k: _f64(inp[k][b]) for k in ("x", "g", "q") if k in inp}
+    d["bias"] = _f64(inp["bias"])
+    if wl.dtype == "mixed":
+        import oracle as O
+        import numpy as np
+        d["kv"] = O.dequantize_rows_e4m3(inp["kv_nope"][b].cpu().view(torch.uint8).numpy(),
+                                         inp["kv_scale"][b].cpu().numpy(),
+                                         inp["kv_rope"][b].cpu().view(torch.int16).numpy().view(np.uint16))
+    else:
+        d["kv"] = _f64(inp["kv"][b])
+    if wl.mode.startswith("csa"):
+        for k in ("xi", "gi", "w"):
+            d[k] = _f64(inp[k][b])
+        d["bias_i"] = _f64(inp["bias_i"])
+        if wl.dtype == "mixed":
+            d["keys"] = _f64(inp["keys"][b]) * inp["keys_scale"][b].cpu().double().numpy()[:, None]
+            d["q_idx"] = _f64(inp["q_idx"][b]) * inp["q_idx_scale"][b].cpu().double().numpy()[..., None]
+        else:
+            d["keys"] = _f64(inp["keys"][b])
+            d["q_idx"] = _f64(inp["q_idx"][b])
+    return d
+
+
+def _oracle_decode_step(wl, d):
+    """The oracle's complete decode step of one sequence: compress the block
+    the token completes into both caches, score every entry, keep the top-k,
+    attend (CSA); compress and attend densely (HCA)."""
+    import numpy as np
+    import oracle as O
     N, m = wl.N, wl.m
-    x, g = f64(inp["x"][b]), f64(inp["g"][b])
-    xi, gi = f64(inp["xi"][b]), f64(inp["gi"][b])
-    kv = np.array(f64(inp["kv"][b]))
-    keys = np.array(f64(inp["keys"][b]))
+    store = "e4m3" if wl.dtype == "mixed" else "bf16"
+    kv = np.array(d["kv"])
     a = (N - 1) * m - wl.raw_pos0
-    kv[N - 1] = O.store_rows(O.compress(x[a:a + m], g[a:a + m], f64(inp["bias"]), m), "bf16")
-    keys[N - 1] = O.store_rows(O.compress(xi[a:a + m], gi[a:a + m], f64(inp["bias_i"]), m), "bf16")
+    kv[N - 1] = O.store_rows(O.compress(d["x"][a:a + m], d["g"][a:a + m], d["bias"], m), store,
+                             wl.D_v)[0]
     pos = np.array([wl.q_pos0])
-    scores = O.index_scores(f64(inp["q_idx"][b]), f64(inp["w"][b]), keys, pos, m)
+    if wl.mode.startswith("hca"):
+        return O.hca_attend(d["q"], kv, d["x"], wl.raw_pos0, pos, m, wl.W, wl.D_v, wl.scale)
+    keys = np.array(d["keys"])
+    keys[N - 1] = O.store_rows(O.compress(d["xi"][a:a + m], d["gi"][a:a + m], d["bias_i"], m),
+                               store)[0]
+    scores = O.index_scores(d["q_idx"], d["w"], keys, pos, m)
     sel = O.topk(scores, pos, m, wl.k)
-    return O.csa_attend(f64(inp["q"][b]), kv, x, wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)
+    return O.csa_attend(d["q"], kv, d["x"], wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """Time the oracle on a bounded sample of the workload (inputs are the
+    same seeded tensors the GPU ran on).  Decode: complete steps of whole
+    sequences until the budget is spent.  Prefill: the compression of the
+    sequence (HCA: of a sample of blocks, scaled by the block count) plus
+    index / top-k / attention of sampled queries, extrapolated to every query
+    by the exact per-query work (flops of the index and attention steps)."""
+    import numpy as np
+    import oracle as O
+    cores = _blas_threads()
+    unit = "tok/s" if wl.mode.endswith("decode") else "query-tok/s"
+    if wl.mode.endswith("decode"):
+        sec, nseq = 0.0, 0
+        while nseq < wl.B and (nseq == 0 or sec < budget_s):
+            d = _seq_inputs(wl, inp, nseq)
+            t0 = time.perf_counter()
+            _oracle_decode_step(wl, d)
+            sec += time.perf_counter() - t0
+            nseq += 1
+        return {"value": nseq / sec, "unit": unit, "cores": cores, "kind": "oracle",
+                "sample": f"{nseq} of {wl.B} sequences, complete decode step each"}
+    m, N, Q = wl.m, wl.N, wl.Q
+    pos_all = wl.q_pos0 + np.arange(Q)
+    nv_all = np.minimum((pos_all + 1) // m, N)
+    win_all = np.minimum(wl.W, pos_all + 1)
+    csa_ = wl.mode.startswith("csa")
+    if csa_:
+        work_all = (nv_all * wl.H_I * wl.d_I * 2
+                    + (np.minimum(wl.k, nv_all) + win_all) * wl.H * (wl.D_qk + wl.D_v) * 2)
+    else:
+        work_all = (nv_all + win_all) * wl.H * (wl.D_qk + wl.D_v) * 2
+    bias = _f64(inp["bias"])
+    if csa_:
+        x, g = _f64(inp["x"][0]), _f64(inp["g"][0])
+        xi, gi = _f64(inp["xi"][0]), _f64(inp["gi"][0])
+        bias_i = _f64(inp["bias_i"])
+        t0 = time.perf_counter()
+        kv = O.store_rows(O.compress(x, g, bias, m), "bf16")
+        keys = O.store_rows(O.compress(xi, gi, bias_i, m), "bf16")
+        t_comp = time.perf_counter() - t0
+        comp_note = "compression of all entries timed whole"
+    else:
+        nb = min(64, N)
+        blocks = np.linspace(0, N - 1, nb).astype(np.int64)
+        rows = torch.from_numpy((blocks[:, None] * m + np.arange(m)[None]).ravel() - wl.raw_pos0)
+        xs = _f64(inp["x"][0][rows.to(inp["x"].device)])
+        gs = _f64(inp["g"][0][rows.to(inp["g"].device)])
+        t0 = time.perf_counter()
+        ents = O.store_rows(O.compress(xs, gs, bias, m), "bf16")
+        t_comp = (time.perf_counter() - t0) * N / nb
+        kv = np.tile(ents, (N // nb + 1, 1))[:N]  # timing only: the sampled blocks' entries, tiled
+        comp_note = f"compression of {nb} of {N} blocks, scaled by the block count"
+    nq = 6
+    qs = np.unique(np.linspace(0, Q - 1, nq).astype(np.int64))
+    sec, work = 0.0, 0.0
+    for i in qs:
+        t = int(pos_all[i])
+        qd = _f64(inp["q"][0][int(i):int(i) + 1])
+        lo = max(0, t - wl.W + 1) - wl.raw_pos0
+        raw = _f64(inp["x"][0][lo:t + 1 - wl.raw_pos0])
+        p = np.array([t])
+        if csa_:
+            qi = _f64(inp["q_idx"][0][int(i):int(i) + 1])
+            wv = _f64(inp["w"][0][int(i):int(i) + 1])
+            t0 = time.perf_counter()
+            sc = O.index_scores(qi, wv, keys, p, m)
+            sel = O.topk(sc, p, m, wl.k)
+            O.csa_attend(qd, kv, raw, lo + wl.raw_pos0, sel, p, wl.W, wl.D_v, wl.scale)
+        else:
+            t0 = time.perf_counter()
+            O.hca_attend(qd, kv, raw, lo + wl.raw_pos0, p, m, wl.W, wl.D_v, wl.scale)
+        sec += time.perf_counter() - t0
+        work += float(work_all[i])
+    est = t_comp + sec / work * float(work_all.sum())
+    return {"value": Q / est, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"extrapolated: {comp_note}; index/top-k/attention of {qs.size} of {Q} "
+                      f"queries, scaled by the exact per-query flop counts",
+            "seconds_timed": t_comp + sec}
 
 
 def _cpu_inputs(wl, nseq):
@@ -117,13 +248,13 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    inp = _cpu_inputs(wl, 1)
+    d = _seq_inputs(wl, _cpu_inputs(wl, 1), 0)
     for _ in range(args.warmup):
-        _oracle_decode_step(wl, inp, 0)
+        _oracle_decode_step(wl, d)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_decode_step(wl, inp, 0)
+        _oracle_decode_step(wl, d)
         times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
     value = 1.0 / sec
@@ -167,11 +298,12 @@ class Clocks:
 
     def __init__(self):
         self.proc = None
-        self.path = ROOT / "gpurun_out" / f"clocks_{os.getpid()}.csv"
+        fd, name = tempfile.mkstemp(prefix="csa_clocks_", suffix=".csv")
+        os.close(fd)
+        self.path = Path(name)
 
     def start(self):
         try:
-            self.path.parent.mkdir(exist_ok=True)
             uuid = None
             try:
                 uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
@@ -195,7 +327,9 @@ class Clocks:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = [r.split(",") for r in self.path.read_text().strip().splitlines() if r.strip()]
+        text = self.path.read_text()
+        self.path.unlink(missing_ok=True)
+        rows = [r.split(",") for r in text.strip().splitlines() if r.strip()]
         rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
         if not rows:
             return None
@@ -250,6 +384,8 @@ def algorithmic_work(wl):
         w["compress_bytes"] = B * new * (m * 2 * (wl.D_qk + wl.d_I) * esz + entry_b + key_b)
         w["index_bytes"] = B * (N * key_b + wl.Q * (qi_b + wl.H_I * 4))
         w["index_flops"] = float(B * nv.sum() * wl.H_I * wl.d_I * 2)
+        # the visible scores read once, the index lists written
+        w["topk_bytes"] = B * (nv.sum() * 4 + wl.Q * wl.k * 4)
         keys = np.minimum(wl.k, nv) + win
         w["attend_flops"] = float(B * keys.sum() * wl.H * (wl.D_qk + wl.D_v) * 2)
         w["attend_bytes"] = B * (np.minimum(wl.k, nv).sum() * entry_b + win.sum() * wl.D_qk * esz
@@ -263,8 +399,23 @@ def algorithmic_work(wl):
     return {k: float(v) for k, v in w.items()}
 
 
+def part_bounds(wl):
+    """The roofline of each timed part of a step: (bound, algorithmic work),
+    bytes for the HBM streams, flops for the tensor-core contractions."""
+    w = algorithmic_work(wl)
+    decode = wl.mode.endswith("decode")
+    b = {"compress": ("hbm", w["compress_bytes"])}
+    if wl.mode.startswith("csa"):
+        b["index"] = ("hbm", w["index_bytes"]) if decode else ("tensor", w["index_flops"])
+        b["topk"] = ("hbm", w["topk_bytes"])
+        b["attend"] = ("hbm", w["attend_bytes"]) if decode else ("tensor", w["attend_flops"])
+    else:
+        b["hca"] = ("hbm", w["hca_bytes"]) if decode else ("tensor", w["hca_flops"])
+    return b
+
+
 def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
-            with_clocks=True):
+            with_clocks=True, want_cpu=False):
     """Time one workload: the whole step as a CUDA graph, each part in a graph
     of its own, and the end-to-end path with host copies."""
     from long_context_sparse_25_b300 import csa, synth
@@ -364,8 +515,22 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     g_full2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_full2, stream=stream):
         step2.run(stream=stream)
-    sets = [(step, g_full, [inp[k] for k in keys_in]), (step2, g_full2, [inp2[k] for k in keys_in])]
-    host_in = [inp[k].cpu().pin_memory() for k in keys_in]
+
+    def new_inputs(d):
+        # What a step brings in: a decode step's new token (its query rows and
+        # its raw KV / indexer-key rows with their gates; the earlier raw rows
+        # of the window arrived with earlier steps and stay resident); every
+        # input of a prefill step.
+        out = []
+        for k in keys_in:
+            t = d[k]
+            if decode and k in ("x", "g", "xi", "gi"):
+                t = t[:, -1:]
+            out.append(t)
+        return out
+
+    sets = [(step, g_full, new_inputs(inp)), (step2, g_full2, new_inputs(inp2))]
+    host_in = [t.cpu().pin_memory() for t in new_inputs(inp)]
     host_out = [torch.empty(st_.out.shape, dtype=st_.out.dtype, pin_memory=True) for st_, _, _ in sets]
     bi = sum(t_.numel() * t_.element_size() for t_ in host_in)
     bo = host_out[0].numel() * host_out[0].element_size()
@@ -406,7 +571,12 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne, dist, dev)
     units = job_units(wl, world)
+    cpu = None
+    if want_cpu:
+        torch.cuda.synchronize()
+        cpu = cpu_baseline(wl, inp)
     res = {"ms": ms, "value": units / (ms / 1e3), "per_part_ms": per_part, "clocks": clk,
+           "cpu_baseline": cpu,
            "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
            "launches_per_step": step.launches_per_step()}
@@ -416,46 +586,48 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     return res
 
 
-def roofline(wl, per_part, peaks, peak_kind):
-    """Roofline of the dominant part: HBM for the decode streams (the CSA
-    indexer over the key cache, the HCA attention over the entry cache), the
-    bf16 tensor peak for the prefill contractions (parts timed alone, so the
-    burst peak applies)."""
-    w = algorithmic_work(wl)
-    if wl.mode == "hca_decode":
-        name = "hca"
-        achieved = w["hca_bytes"] / (per_part[name] / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
-                "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _traffic(f"{name}:{wl.name}"), "algorithmic_bytes_per_launch": w["hca_bytes"],
-                "tensor_frac": w["hca_flops"] / (per_part[name] / 1e3) / 1e12 / peaks["bf16_tflops"]}
-    if wl.mode == "hca_prefill":
-        name = "hca"
-        achieved = w["hca_flops"] / (per_part[name] / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
-                "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
-                "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-                "traffic": _traffic(f"{name}:{wl.name}"), "algorithmic_flops_per_launch": w["hca_flops"]}
-    if wl.mode == "csa_decode":
-        name = "index"
-        achieved = w["index_bytes"] / (per_part[name] / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
-                "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _traffic(f"index_tc_kernel:{wl.name}"),
-                "algorithmic_bytes_per_launch": w["index_bytes"]}
-    name = max(("index", "attend"), key=lambda k: per_part[k])
-    achieved = w[f"{name}_flops"] / (per_part[name] / 1e3) / 1e12
-    peak = peaks["bf16_tflops"]
-    return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
-            "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s", "frac": achieved / peak,
-            "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-            "traffic": _traffic(f"{name}:{wl.name}"),
-            "algorithmic_flops_per_launch": w[f"{name}_flops"],
-            "other_part": {k: (w[f"{k}_flops"] / (per_part[k] / 1e3) / 1e12) / peak
-                           for k in ("index", "attend") if k != name}}
+def roofline(wl, per_part, ms_step, peaks, peak_kind):
+    """Roofline of the part that takes the longest (each part timed alone in a
+    graph of its own, so the burst peaks apply), every part's fraction, and
+    the step's: all algorithmic bytes (decode) or flops (prefill) of the step
+    over the time of the whole step."""
+    bounds = part_bounds(wl)
+
+    def frac_of(bound, amount, ms):
+        if bound == "hbm":
+            ach = amount / (ms / 1e3) / 1e9
+            return ach, peaks["hbm_gbs"], "GB/s"
+        ach = amount / (ms / 1e3) / 1e12
+        return ach, peaks["bf16_tflops"], "TFLOP/s"
+
+    name = max(per_part, key=lambda k: per_part[k])
+    bound, amount = bounds[name]
+    ach, peak, unit = frac_of(bound, amount, per_part[name])
+    r = {"bound": bound, "kernel": name, "achieved": ach, "peak": peak, "unit": unit,
+         "frac": ach / peak, "traffic": _traffic(f"{name}:{wl.name}"),
+         "peak_kind": f"{peak_kind} " + ("HBM copy" if bound == "hbm" else "bf16 burst"),
+         ("algorithmic_bytes_per_launch" if bound == "hbm" else "algorithmic_flops_per_launch"): amount}
+    if bound == "tensor":
+        r["frac_sustained"] = ach / peaks["bf16_tflops_sustained"]
+        r["frac_nominal"] = ach / NOMINAL_BF16_TFLOPS
+    r["parts"] = {}
+    for k, t in per_part.items():
+        b_, a_ = bounds[k]
+        x, p_, u_ = frac_of(b_, a_, t)
+        r["parts"][k] = {"bound": b_, "ms": t, "achieved": x, "unit": u_, "frac": x / p_}
+    if wl.mode.endswith("decode"):
+        tot_b = sum(a_ for b_, a_ in bounds.values())
+        ach = tot_b / (ms_step / 1e3) / 1e9
+        r["step"] = {"bound": "hbm", "algorithmic_bytes": tot_b, "achieved": ach, "unit": "GB/s",
+                     "peak": peaks["hbm_gbs"], "frac": ach / peaks["hbm_gbs"]}
+    else:
+        tot_f = sum(a_ for b_, a_ in bounds.values() if b_ == "tensor")
+        ach = tot_f / (ms_step / 1e3) / 1e12
+        r["step"] = {"bound": "tensor", "algorithmic_flops": tot_f, "achieved": ach,
+                     "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                     "frac": ach / peaks["bf16_tflops"],
+                     "frac_sustained": ach / peaks["bf16_tflops_sustained"]}
+    return r
 
 
 def run_ours(args, wl):
@@ -472,19 +644,23 @@ def run_ours(args, wl):
         dist.init_process_group("nccl", device_id=dev)
     peaks, peak_kind = _peaks()
 
-    head = measure(args, wl, dev, dist, world, rank)
+    # the oracle's timed baseline: rank 0 of a one-GPU run only
+    want_cpu = world == 1 and rank == 0 and not args.no_cpu_baseline
+    head = measure(args, wl, dev, dist, world, rank, want_cpu=want_cpu)
 
     def secondary(name, steps):
         sw = synth.WORKLOADS[name]
         sargs = argparse.Namespace(**vars(args))
         sargs.steps = steps
-        r = measure(sargs, sw, dev, dist, world, rank, e2e_steps=min(steps, 5), with_clocks=False)
+        r = measure(sargs, sw, dev, dist, world, rank, e2e_steps=min(steps, 5), with_clocks=False,
+                    want_cpu=want_cpu)
         dec = sw.mode.endswith("decode")
         return {"workload": _config(sw)["workload"], "value": r["value"],
                 "unit": "tok/s" if dec else "query-tok/s", "ms_per_step": r["ms"],
                 "steps": steps, "per_part_ms": r["per_part_ms"],
-                "roofline": roofline(sw, r["per_part_ms"], peaks, peak_kind),
-                "e2e": r["e2e"], "gpu_launches": r["launches_per_step"] * steps}
+                "roofline": roofline(sw, r["per_part_ms"], r["ms"], peaks, peak_kind),
+                "e2e": r["e2e"], "gpu_launches": r["launches_per_step"] * steps,
+                "cpu_baseline": r["cpu_baseline"]}
 
     prefill = None
     others = {}
@@ -499,24 +675,14 @@ def run_ours(args, wl):
         if dist:
             dist.destroy_process_group()
         return
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline and wl.mode == "csa_decode":
-        nseq = 2
-        cinp = _cpu_inputs(wl, nseq)
-        t0 = time.perf_counter()
-        for b in range(nseq):
-            _oracle_decode_step(wl, cinp, b)
-        sec = time.perf_counter() - t0
-        cpu = {"value": nseq / sec, "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
-               "sample": f"{nseq} of {wl.B} sequences, complete decode step each "
-                         f"(compress tail, index {wl.N} entries, top-{wl.k}, attend)"}
+    cpu = head["cpu_baseline"]
     decode = wl.mode.endswith("decode")
     line = {
         "metric": METRIC, "value": head["value"], "unit": "tok/s" if decode else "query-tok/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": _config(wl),
-        "roofline": roofline(wl, head["per_part_ms"], peaks, peak_kind),
+        "roofline": roofline(wl, head["per_part_ms"], head["ms"], peaks, peak_kind),
         "per_part_ms": head["per_part_ms"],
         "timing": "CUDA graph of the whole step replayed per timed step; CUDA events on the "
                   "launching stream; each part timed alone in a graph of its own for the roofline",

@@ -8,8 +8,8 @@
  *            "V3 看家本领一：MLA" (latent + decoupled RoPE key row layout).
  *   [yudong] "DeepSeek-V4 详解", section 2.2 Steps 1-4 (CSA) and section 2.3
  *            Steps 1-2 (HCA).
- *   [jaylab] "DeepSeek-V4 — 百万 Token 上下文的高效 MoE 模型", bullet
- *            "KV cache 混合精度 — RoPE 维度 BF16，其余 FP8".
+ *   [jaylab] "DeepSeek-V4 — 百万 Token 上下文的高效 MoE 模型", section
+ *            "其他技术细节" (the bullet on the mixed BF16 / FP8 KV cache).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -36,7 +36,8 @@
  *           threads; two calls that write the same buffer race.
  * Determinism. For fixed inputs every output is bitwise reproducible and
  *           independent of the batch size and of the slot a sequence takes
- *           in the batch ([csdn] V4 的其他升级, 确定性 kernel).
+ *           in the batch ([csdn] section "V4 的其他升级", the bullet on
+ *           deterministic kernels).
  */
 #ifndef CSA_B300_H
 #define CSA_B300_H
@@ -70,7 +71,7 @@ typedef enum {
  * A block of rows (compressed entries, raw tokens or indexer keys), one
  * sequence after the other: row r of sequence b is element [b, r].
  *   dtype F32 / BF16: `data` is [B, n_rows, width]; rope, scale unused (NULL).
- *   dtype E4M3 (mixed layout, [jaylab] KV cache 混合精度): the first `nope`
+ *   dtype E4M3 (mixed layout, [jaylab] "其他技术细节"): the first `nope`
  *       channels of each row are e4m3 codes in `data` [B, n_rows, nope] with
  *       one fp32 scale per row in `scale` [B, n_rows] (value = code * scale);
  *       the remaining width - nope channels (the RoPE dims) are bfloat16 in
@@ -102,7 +103,8 @@ typedef struct {
 
 /*
  * csa_compress -- pool every m adjacent raw rows into one entry
- * ([csdn] V4 改进一 CSA 第一步; [yudong] 2.2 Step 1, 2.3 Step 1):
+ * ([csdn] section "V4 改进一：CSA 与 HCA", first CSA step; [yudong] 2.2
+ * Step 1, 2.3 Step 1):
  *   E[b,s,c] = sum_{i<m} softmax_i(gate[b,sm+i,c] + bias[i,c]) * x[b,sm+i,c]
  * (softmax over the m positions, separately for every channel c).
  *
@@ -127,8 +129,8 @@ int csa_compress(const void* x, const void* gate, csa_dtype in_dtype, const floa
                  int64_t s_end, const csa_rows* out, csa_stream_t stream);
 
 /*
- * csa_index -- lightning indexer scores ([csdn] V4 改进一 "闪电索引器";
- * [yudong] 2.2 Step 2):
+ * csa_index -- lightning indexer scores ([csdn] section "V4 改进一：CSA 与
+ * HCA", second CSA step; [yudong] 2.2 Step 2):
  *   I[b,i,s] = sum_{j<H_I} w[b,i,j] * max(0, q_idx[b,i,j,:] . keys[b,s,:])
  * for s < min(N, n_vis(q_pos0+i)); -inf for every other s < N.
  *
@@ -148,8 +150,8 @@ int csa_index(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const f
               float* scores, csa_stream_t stream);
 
 /*
- * csa_topk -- keep the best entries per query ([csdn] "只取分数最高的 top-k 条";
- * [yudong] 2.2 Step 3):
+ * csa_topk -- keep the best entries per query ([csdn] section "V4 改进一：CSA
+ * 与 HCA", second CSA step; [yudong] 2.2 Step 3):
  *   idx[b,i,:] = the min(k, n_vis) indices s < n_vis = min(N, n_vis(q_pos0+i))
  *   with the largest scores[b,i,s], ascending, then -1 up to k.
  * Ties go to the lower index; -0.0 and +0.0 are equal.  Scores must not be
@@ -176,11 +178,16 @@ int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, in
  *   - Sizes whose scratch (csa_workspace_size(p, CSA_WS_TOPK, Q, N)) exceeds
  *     CSA_TOPK_NOALLOC_MAX_BYTES are rejected with CSA_ERR_WORKSPACE.
  *   - The first call on a device looks up the array's device address on that
- *     device (it must be the current device); make that first call before
- *     any stream capture.
- *   - All calls share the one array and the call re-zeroes what must start
- *     at zero, but calls that overlap on the GPU (other streams, other host
- *     threads) race on it: serialise them.
+ *     device (it must be the current device) and keeps it for the life of
+ *     the process; make that first call before any stream capture.  The
+ *     kept address assumes the device's primary context: after
+ *     cudaDeviceReset, or with another driver-API context made current, the
+ *     library's module may sit at another address, and this call must not
+ *     be used.
+ *   - All calls share the one array.  Each call writes every scratch byte it
+ *     later reads before reading it, so nothing carries over from an earlier
+ *     call; but calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array: serialise them.
  */
 #define CSA_TOPK_NOALLOC_MAX_BYTES (16u << 20)
 
@@ -189,8 +196,9 @@ int csa_topk_noalloc(const csa_params* p, const float* scores, int64_t q_pos0, i
 
 /*
  * csa_attend -- shared-KV (MQA) attention of every query head over the
- * selected entries plus the raw window ([csdn] "保留一小段最近距离的原始 KV
- * （滑动窗口）…注意力用共享 KV 的 MQA 形式"; [yudong] 2.2 Step 4):
+ * selected entries plus the raw window ([csdn] section "V4 改进一：CSA 与
+ * HCA": recent raw KV in a sliding window, one KV shared by all heads;
+ * [yudong] 2.2 Step 4):
  *   keys K = { kv[b,s] : s in idx[b,i,:], s >= 0 } ++ { raw token u in window(t) }
  *   out[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . K_j) * K_j[0:D_v]
  * (the value is the leading D_v channels of the key row: the latent of
@@ -212,8 +220,8 @@ int csa_attend(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_
                csa_stream_t stream);
 
 /*
- * hca_attend -- HCA dense attention ([csdn] HCA "直接做密集注意力"; [yudong] 2.3
- * Step 2): as csa_attend with the key set every visible entry
+ * hca_attend -- HCA dense attention ([csdn] section "V4 改进一：CSA 与 HCA",
+ * the HCA paragraph; [yudong] 2.3 Step 2): as csa_attend with the key set every visible entry
  * s < min(N, n_vis(t)) (p->m is the HCA block size, e.g. 128; p->k and the
  * indexer fields are ignored) followed by the raw window.
  */

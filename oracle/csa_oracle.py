@@ -15,11 +15,12 @@ Sources ("page title", section):
            section "V4 改进一：CSA 与 HCA"; MLA layout in "V3 看家本领一：MLA".
   [yudong] "DeepSeek-V4 详解", section 2.2 Steps 1-4 (CSA), section 2.3
            Steps 1-2 (HCA).
-  [jaylab] "DeepSeek-V4 — 百万 Token 上下文的高效 MoE 模型", bullets
-           "RMSNorm 直接应用于 attention queries/KV entries" and
-           "KV cache 混合精度 — RoPE 维度 BF16，其余 FP8".
+  [jaylab] "DeepSeek-V4 — 百万 Token 上下文的高效 MoE 模型", section
+           "3. Muon 优化器" (the bullet on RMSNorm of the attention queries and
+           KV entries) and section "其他技术细节" (the bullet on the mixed
+           BF16 / FP8 KV cache).
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
   * compression is a per-channel softmax over the m positions of
     (gate logit + bias[i]); the projections that produce X and the gates are
     upstream inputs;
@@ -158,7 +159,8 @@ def quantize_rows_e4m3(v: np.ndarray, nope: int) -> dict:
     """Mixed-precision row storage: the first ``nope`` channels in E4M3 with one
     float32 scale per row, the remaining (RoPE) channels in bfloat16.
 
-    [jaylab] "KV cache 混合精度 — RoPE 维度 BF16，其余 FP8".  Reading: the scale
+    [jaylab] section "其他技术细节", the KV-cache bullet: RoPE dims stay in
+    BF16, the other dims are stored in FP8.  Reading: the scale
     is amax / 448 over the nope channels, rounded to float32 (1.0 for an
     all-zero row); each code is the E4M3 rounding, taken directly from float64,
     of value / scale.
@@ -198,9 +200,9 @@ def store_rows(v: np.ndarray, dtype: str, nope: int | None = None) -> np.ndarray
 
 
 # ---------------------------------------------------------------------------
-# Step 1: compression  ([csdn] V4 改进一 "每 m 个相邻 token 的 KV，用一组带位置偏置的
-# softmax 权重压成 1 条"; [yudong] 2.2 Step 1 "softmax-gated pooling + 学习位置
-# bias", 2.3 Step 1 for m' = 128)
+# Step 1: compression ([csdn] section "V4 改进一：CSA 与 HCA", the first CSA
+# step: m adjacent tokens pooled into one entry by softmax weights that carry
+# a position bias; [yudong] 2.2 Step 1, and 2.3 Step 1 for m' = 128)
 # ---------------------------------------------------------------------------
 
 def compress_weights(g: np.ndarray, bias: np.ndarray, m: int) -> np.ndarray:
@@ -224,8 +226,9 @@ def compress(x: np.ndarray, g: np.ndarray, bias: np.ndarray, m: int) -> np.ndarr
 
 
 # ---------------------------------------------------------------------------
-# Step 2: lightning indexer ([csdn] "一个轻量的'闪电索引器'给每条压缩 KV 与当前
-# query 的相关性打分"; [yudong] 2.2 Step 2)
+# Step 2: lightning indexer ([csdn] section "V4 改进一：CSA 与 HCA", the second
+# CSA step: a light indexer scores each compressed entry against the query;
+# [yudong] 2.2 Step 2)
 # ---------------------------------------------------------------------------
 
 def n_vis(t, m: int):
@@ -254,7 +257,8 @@ def index_scores(q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray,
 
 
 # ---------------------------------------------------------------------------
-# Step 3: top-k ([csdn] "只取分数最高的 top-k 条进入注意力"; [yudong] 2.2 Step 3)
+# Step 3: top-k ([csdn] section "V4 改进一：CSA 与 HCA": only the k best-scoring
+# entries go on to attention; [yudong] 2.2 Step 3)
 # ---------------------------------------------------------------------------
 
 def topk_row(scores: np.ndarray, nv: int, k: int) -> np.ndarray:
@@ -289,8 +293,9 @@ def topk(scores: np.ndarray, q_pos: np.ndarray, m: int, k: int) -> np.ndarray:
 
 # ---------------------------------------------------------------------------
 # Step 4: shared-KV MQA over the kept entries plus the raw window
-# ([csdn] "再保留一小段最近距离的原始 KV（滑动窗口）…注意力用共享 KV 的 MQA 形式";
-# [yudong] 2.2 Step 4, 2.3 Step 2; value = latent part, as in [csdn] MLA)
+# ([csdn] section "V4 改进一：CSA 与 HCA": a short sliding window of recent raw
+# KV is kept uncompressed, and attention is MQA over one shared KV; [yudong]
+# 2.2 Step 4, 2.3 Step 2; value = latent part, as in [csdn] MLA)
 # ---------------------------------------------------------------------------
 
 def window_range(t: int, W: int) -> tuple[int, int]:
@@ -336,7 +341,8 @@ def csa_attend(q, entries, raw, raw_pos0: int, sel, q_pos, W: int, D_v: int,
 def hca_attend(q, entries, raw, raw_pos0: int, q_pos, m: int, W: int, D_v: int,
                scale: float) -> np.ndarray:
     """HCA attention for one sequence: every visible entry (no selection) plus
-    the raw window ([csdn] HCA "直接做密集注意力"; [yudong] 2.3 Step 2)."""
+    the raw window ([csdn] section "V4 改进一：CSA 与 HCA": HCA entries are few
+    enough to attend to all of them; [yudong] 2.3 Step 2)."""
     q = np.asarray(q, dtype=np.float64)
     Q, H, _ = q.shape
     out = np.zeros((Q, H, D_v))

@@ -149,18 +149,25 @@ def check_selection(sel_gpu: np.ndarray, ref_scores: np.ndarray, nvis: np.ndarra
     return swaps
 
 
-def check_out(gpu: np.ndarray, ref: np.ndarray, f32: bool):
+def check_out(gpu: np.ndarray, ref: np.ndarray, f32: bool, unit_scale: bool = True):
+    """Output parity.  fp32: relative Frobenius error <= 1e-4.  bf16 / fp8:
+    relative Frobenius error <= 2e-2 and max-abs error <= 5e-2, the bound
+    stated for unit-scale outputs.
+
+    unit_scale=False is for outputs that are not unit-scale: the x20 outliers
+    of the mixed-precision workload (|o| up to ~60) and crafted keys that grow
+    along the list.  There a single bf16 rounding of the output is already
+    2^-9 |o|, so the max-abs bound becomes 5e-2 + 2^-8 |o| (one bf16 ulp on top
+    of the unit-scale bound)."""
     num = np.linalg.norm((gpu - ref).ravel())
     den = np.linalg.norm(ref.ravel()) + 1e-30
     fro = num / den
-    # The 5e-2 max-abs bound is for unit-scale outputs.  Outputs that carry
-    # the x20 outliers of the mixed-precision workload reach |o| ~ 60, where a
-    # single bf16 rounding of the output is already 2^-9 |o|; the bound is
-    # therefore 5e-2 + 2^-8 |o| (one bf16 ulp on top of the unit-scale bound).
-    excess = np.abs(gpu - ref) - 2.0 ** -8 * np.abs(ref)
-    mx = float(excess.max()) if gpu.size else 0.0
+    err = np.abs(gpu - ref)
+    if not unit_scale:
+        err = err - 2.0 ** -8 * np.abs(ref)
+    mx = float(err.max()) if gpu.size else 0.0
     if f32:
         assert fro <= FRO_F32, f"relative Frobenius error {fro:.3e} > {FRO_F32}"
     else:
-        assert fro <= FRO_BF16 and mx <= MAXABS_BF16, f"fro {fro:.3e}, max-abs excess {mx:.3e}"
+        assert fro <= FRO_BF16 and mx <= MAXABS_BF16, f"fro {fro:.3e}, max-abs error {mx:.3e}"
     return fro, mx

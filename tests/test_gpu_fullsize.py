@@ -1,10 +1,12 @@
 """Parity at the full size of the timed workloads, in the launch configuration
 bench.py times.  CSA decode at 1M-token context, B = 32 (262,144 entries per
-sequence, one csa_forward per step): every sequence's compressed tail entry
-and key bit-exact, every visible score within 1e-5 of the row scale, the
-selection within the swap rule; the attention output on a fixed sample of 8
-sequences (the oracle evaluates the 1152 keys each query keeps).  CSA prefill
-at 64K tokens and HCA prefill at 1M tokens on fixed query samples."""
+sequence, one csa_forward per step) and mixed-precision CSA decode at 512K,
+B = 64: every sequence's compressed tail entry and key bit-exact, every
+visible score within 1e-5 of the row scale, the selection within the swap
+rule; the attention output on a fixed sample of 8 sequences (the oracle
+evaluates the 1152 keys each query keeps).  HCA decode at 1M, B = 32: every
+sequence.  CSA prefill at 64K tokens and HCA prefill at 1M tokens on fixed
+query samples."""
 
 import numpy as np
 import pytest
@@ -68,12 +70,55 @@ def _decode_parity(wl, dev, attn_seqs):
                 assert np.array_equal(ent[last[0]], new_kv[0]), f"seq {b}: tail entry"
             o = O.csa_attend(f64(inp["q"][b]), ent, x, wl.raw_pos0, np.arange(s.size)[None], pos,
                              wl.W, wl.D_v, wl.scale)
-            check_out(out[b], o, False)
+            check_out(out[b], o, False, unit_scale=wl.outliers == 0)
 
 
 def test_decode_1m_full_size(cuda_device):
     wl = synth.WORKLOADS["csa_decode_1m"]
     _decode_parity(wl, cuda_device, attn_seqs={0, 5, 11, 16, 21, 26, 30, 31})
+
+
+def test_decode_fp8_512k_full_size(cuda_device):
+    """Mixed-precision CSA decode at 512K context, B = 64 (131,072 entries per
+    sequence, e4m3 nope dims with a row scale, bf16 RoPE dims, e4m3 indexer
+    keys and queries, 1% x20 outliers), in the launch configuration bench.py
+    times: rows above 16,384 entries take the multi-CTA top-k, and the e4m3
+    indexer runs its full schedule.  Every sequence's tail entry and key equal
+    the oracle's (quantised from float64), every visible score within 1e-5 of
+    the row scale, the selection within the swap rule; attention on a fixed
+    sample of 8 sequences."""
+    wl = synth.WORKLOADS["csa_decode_fp8_512k"]
+    _decode_parity(wl, cuda_device, attn_seqs={0, 9, 18, 27, 36, 45, 54, 63})
+
+
+def test_hca_decode_1m_full_size(cuda_device):
+    """HCA decode at 2^20 tokens, B = 32 (8,192 entries of m' = 128 raw rows per
+    sequence), in the launch configuration bench.py times (csa_compress of the
+    block the token completes, then hca_attend): the key list of 8,192 entries
+    plus 128 window rows is 65 tiles, cut into split runs whose full tiles of
+    consecutive entries load as TMA boxes, merged by the combine kernel.  Every
+    sequence's tail entry within one bf16 ulp of the oracle's and every
+    sequence's attention output checked."""
+    wl = synth.WORKLOADS["hca_decode_1m"]
+    dev = cuda_device
+    inp = synth.make_inputs(wl, dev)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    csa.device_status()  # no bounded device-side wait gave up
+    N, m = wl.N, wl.m
+    pos = np.array([wl.q_pos0])
+    out = f64(step.out)
+    bias = f64(inp["bias"])
+    for b in range(wl.B):
+        x, g = f64(inp["x"][b]), f64(inp["g"][b])
+        a = (N - 1) * m - wl.raw_pos0
+        tail = O.compress(x[a:a + m], g[a:a + m], bias, m)[0]
+        kv = f64(inp["kv"][b])
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(tail), 1e-30))) - 7)
+        assert np.all(np.abs(kv[N - 1] - tail) <= ulp + 1e-6), f"seq {b}: tail entry off by > 1 ulp"
+        o = O.hca_attend(f64(inp["q"][b]), kv, x, wl.raw_pos0, pos, m, wl.W, wl.D_v, wl.scale)
+        check_out(out[b], o, False)
 
 
 def test_prefill_64k_full_size(cuda_device):

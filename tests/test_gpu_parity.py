@@ -87,7 +87,7 @@ def test_csa_forward_matches_oracle(case, cuda_device):
         check_scores(scores[b, qs], ref_scores)
         check_selection(sel[b, qs], ref_scores, O.n_vis(o.positions(qs), wl.m), wl.k)
         ref_out = o.attend(qs, sel[b, qs])
-        check_out(out[b, qs], ref_out, wl.dtype == "f32")
+        check_out(out[b, qs], ref_out, wl.dtype == "f32", unit_scale=wl.outliers == 0)
 
 
 HCA_CASES = {
@@ -263,4 +263,4 @@ def test_attend_rescale_holes_and_order(Q, dense, cuda_device):
             ref = O.hca_attend(qv, kvv, rawv, raw_pos0, pos, 1, W, Dv, scale)
         else:
             ref = O.csa_attend(qv, kvv, rawv, raw_pos0, idx[b], pos, W, Dv, scale)
-        check_out(got[b], ref, False)
+        check_out(got[b], ref, False, unit_scale=False)  # keys grow to ~14x unit scale

@@ -328,3 +328,91 @@ def test_pipeline_selects_exactly_k_visible_entries():
         s = sel[t][sel[t] >= 0]
         assert s.size == min(k, nv)
         assert np.all(s < nv)
+
+
+# ------------------------------------------- raw-row offset and the cache path
+def test_window_rows_taken_by_absolute_position_when_raw_starts_late():
+    """Raw rows that start at position raw_pos0 > 0: query t's window is the
+    rows of absolute positions t-W+1 .. t.  The keys are assembled here by
+    absolute position from the full token array and the result compared with
+    torch's scaled_dot_product_attention; the oracle is given only the rows
+    from raw_pos0 on."""
+    T, W, D, D_v, H, scale = 40, 6, 10, 7, 3, 0.35
+    x = rng.standard_normal((T, D))            # rows of absolute positions 0..T-1
+    e = rng.standard_normal((9, D))            # cache entries
+    pos = np.arange(30, T)
+    q = rng.standard_normal((pos.size, H, D))
+    sel = np.stack([np.sort(rng.choice(9, size=4, replace=False)) for _ in pos])
+    r0 = 25                                    # first window row any query needs
+    got = O.csa_attend(q, e, x[r0:], r0, sel, pos, W, D_v, scale)
+    got_h = O.hca_attend(q, e, x[r0:], r0, pos, 4, W, D_v, scale)
+    for i, t in enumerate(pos):
+        win = x[t - W + 1: t + 1]
+        keys = np.concatenate([e[sel[i]], win])
+        ref = _sdpa(q[i:i + 1], keys, keys[:, :D_v], scale)
+        np.testing.assert_allclose(got[i:i + 1], ref, rtol=1e-12, atol=1e-13)
+        keys_h = np.concatenate([e[: (t + 1) // 4], win])  # entries ending at or before t
+        ref_h = _sdpa(q[i:i + 1], keys_h, keys_h[:, :D_v], scale)
+        np.testing.assert_allclose(got_h[i:i + 1], ref_h, rtol=1e-12, atol=1e-13)
+    # the same rows through a view that starts at position 0 give bitwise the same result
+    assert np.array_equal(got, O.csa_attend(q, e, x, 0, sel, pos, W, D_v, scale))
+    assert np.array_equal(got_h, O.hca_attend(q, e, x, 0, pos, 4, W, D_v, scale))
+
+
+def test_pipeline_reads_cached_entries_and_compresses_only_new_ones():
+    """m = 1 (compression is the identity), W = 0, k >= entries: query t attends
+    densely over entries 0..t.  Entries below n_cached must come from the
+    caches (arbitrary rows here, unrelated to the raw rows) and the rest from
+    the raw rows, which start at raw_pos0 > 0.  Checked against torch's
+    scaled_dot_product_attention on keys assembled by hand."""
+    T, D, D_v, H, dI, scale = 20, 8, 6, 2, 4, 0.4
+    n_cached, r0 = 12, 12
+    x_abs = rng.standard_normal((T, D))
+    xi_abs = rng.standard_normal((T, dI))
+    kv_cache = rng.standard_normal((T, D))
+    key_cache = rng.standard_normal((T, dI))
+    pos = np.arange(16, T)
+    q = rng.standard_normal((pos.size, H, D))
+    q_idx = rng.standard_normal((pos.size, 3, dI))
+    w = rng.uniform(0, 1, (pos.size, 3))
+    out, sel, scores = O.csa_pipeline(
+        x=x_abs[r0:], g=rng.standard_normal((T - r0, D)), bias=np.zeros((1, D)),
+        xi=xi_abs[r0:], gi=rng.standard_normal((T - r0, dI)), bias_i=np.zeros((1, dI)),
+        q=q, q_idx=q_idx, w=w, m=1, k=T, W=0, D_v=D_v, scale=scale, q_pos=pos, raw_pos0=r0,
+        kv_cache=kv_cache, key_cache=key_cache, n_cached=n_cached, kv_dtype="f64",
+        key_dtype="f64")
+    ents = np.concatenate([kv_cache[:n_cached], x_abs[n_cached:]])
+    keys = np.concatenate([key_cache[:n_cached], xi_abs[n_cached:]])
+    for i, t in enumerate(pos):
+        assert np.array_equal(sel[i][sel[i] >= 0], np.arange(t + 1))
+        ref = _sdpa(q[i:i + 1], ents[: t + 1], ents[: t + 1, :D_v], scale)
+        np.testing.assert_allclose(out[i:i + 1], ref, rtol=1e-12, atol=1e-13)
+        # indexer scores of the visible entries: keys from the cache, then the new rows
+        dots = np.maximum(q_idx[i] @ keys[: t + 1].T, 0.0)
+        np.testing.assert_allclose(scores[i, : t + 1], w[i] @ dots, rtol=1e-12, atol=1e-13)
+
+
+def test_pipeline_with_a_filled_cache_equals_the_run_without_one():
+    """m = 4, bf16 caches, window 5: running the pipeline on all raw rows from
+    position 0 equals running it with the first n_cached entries already in
+    the caches and only the raw rows from position n_cached*m on."""
+    T, m, D, dI, H = 64, 4, 8, 4, 2
+    x, g = rng.standard_normal((T, D)), rng.standard_normal((T, D))
+    xi, gi = rng.standard_normal((T, dI)), rng.standard_normal((T, dI))
+    bias, bias_i = 0.1 * rng.standard_normal((m, D)), 0.1 * rng.standard_normal((m, dI))
+    pos = np.arange(50, T)
+    q = rng.standard_normal((pos.size, H, D))
+    q_idx, w = rng.standard_normal((pos.size, 3, dI)), rng.uniform(0, 1, (pos.size, 3))
+    kw = dict(bias=bias, bias_i=bias_i, q=q, q_idx=q_idx, w=w, m=m, k=5, W=5, D_v=6, scale=0.3,
+              q_pos=pos, kv_dtype="bf16", key_dtype="bf16")
+    full = O.csa_pipeline(x=x, g=g, xi=xi, gi=gi, **kw)
+    n_cached = 11  # entries 0..10 pool tokens 0..43
+    r0 = n_cached * m
+    kv_cache = np.zeros((T // m, D))
+    key_cache = np.zeros((T // m, dI))
+    kv_cache[:n_cached] = O.store_rows(O.compress(x[:r0], g[:r0], bias, m), "bf16")
+    key_cache[:n_cached] = O.store_rows(O.compress(xi[:r0], gi[:r0], bias_i, m), "bf16")
+    part = O.csa_pipeline(x=x[r0:], g=g[r0:], xi=xi[r0:], gi=gi[r0:], raw_pos0=r0,
+                          kv_cache=kv_cache, key_cache=key_cache, n_cached=n_cached, **kw)
+    for a, b in zip(full, part):
+        assert np.array_equal(a, b)

@@ -3,8 +3,9 @@ the point of the call (code inside a host framework that owns every device
 allocation, or a path that must not call cudaMalloc because it can
 synchronise the device).  Its scratch is a static device array inside the
 library.  Through the C ABI, its index lists must equal those of csa_topk
-given a caller workspace, bit for bit, on two calls in a row (the second
-call must not see anything the first left in the shared array).  Sizes
+given a caller workspace and the oracle's top-k on the same scores, bit for
+bit, on two calls in a row (the second call must not see anything the first
+left in the shared array).  Sizes
 beyond the array are rejected with CSA_ERR_WORKSPACE.
 
 This file is collected last on purpose, and it passes both alone in a fresh
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from long_context_sparse_25_b300 import csa
 
 pytestmark = pytest.mark.gpu
@@ -42,9 +44,13 @@ def test_noalloc_topk_equals_workspace_topk_twice(cuda_device):
         csa.topk_noalloc(p, s, q_pos0, got)
         torch.cuda.synchronize()
         assert torch.equal(got, ref), f"call {call}: index lists differ"
-        # the selection is the k largest scores, ascending
+        # and both are the oracle's selection on the same fp32 scores: the k
+        # largest, ties to the lower index, ascending
         g = got.cpu().numpy()
-        assert np.all(np.diff(g, axis=-1) > 0)
+        s64 = s.cpu().double().numpy()
+        for b in range(B):
+            want = O.topk(s64[b], np.array([q_pos0]), m, k)
+            assert np.array_equal(g[b], want), f"call {call}, sequence {b}: not the oracle's top-k"
 
 
 def test_noalloc_topk_rejects_sizes_beyond_the_static_buffer(cuda_device):
