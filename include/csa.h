@@ -287,6 +287,24 @@ size_t csa_workspace_size(const csa_params* p, int which, int Q, int64_t N);
  */
 int csa_device_status(csa_stream_t stream);
 
+/*
+ * csa_debug_stall_next -- test aid for the failure path of the bounded
+ * device-side waits.  Arms a one-shot: the next launch of the named
+ * tensor-core kernel (CSA_STALL_INDEX: the indexer of csa_index /
+ * csa_forward; CSA_STALL_ATTEND: the attention of csa_attend / hca_attend /
+ * csa_forward) makes its first CTA's MMA issuer wait, while that CTA's first
+ * loads are in flight, on a device flag that nothing sets.  The wait gives up
+ * after 0.1 s through the same path as any wait that runs out: it records
+ * its site, every other wait of the launch gives up, each CTA lets its own
+ * copies and MMAs in flight land and exits.  The next csa_device_status then
+ * returns CSA_ERR_TIMEOUT; the outputs of that launch are not valid, and the
+ * following calls run normally.  Process-wide; 0 disarms.  Not for use in
+ * production: it exists so that tests can observe the timeout report.
+ * Errors: INVALID_ARG (unknown kernel).
+ */
+enum { CSA_STALL_INDEX = 1, CSA_STALL_ATTEND = 2 };
+int csa_debug_stall_next(int kernel);
+
 /* Message describing the last error returned on the calling thread ("" if none). */
 const char* csa_last_error(void);
 

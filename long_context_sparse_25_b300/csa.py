@@ -20,6 +20,7 @@ HEADER = _PKG.parent / "include" / "csa.h"
 
 F32, BF16, E4M3 = 0, 1, 2
 WS_TOPK, WS_ATTEND, WS_HCA, WS_FORWARD = 0, 1, 2, 3
+STALL_INDEX, STALL_ATTEND = 1, 2
 STATUS = {0: "CSA_OK", -1: "CSA_ERR_INVALID_ARG", -2: "CSA_ERR_UNSUPPORTED", -3: "CSA_ERR_ALIGNMENT",
           -4: "CSA_ERR_WORKSPACE", -5: "CSA_ERR_CUDA", -6: "CSA_ERR_TIMEOUT"}
 
@@ -82,6 +83,8 @@ lib.csa_workspace_size.argtypes = [C.POINTER(Params), _I, _I, _I64]
 lib.csa_workspace_size.restype = C.c_size_t
 lib.csa_device_status.argtypes = [_P]
 lib.csa_device_status.restype = C.c_int
+lib.csa_debug_stall_next.argtypes = [_I]
+lib.csa_debug_stall_next.restype = C.c_int
 lib.csa_last_error.argtypes = []
 lib.csa_last_error.restype = C.c_char_p
 
@@ -207,6 +210,12 @@ def forward_args(*, x, gate, bias, xi, gate_i, bias_i, raw_pos0, q, q_idx, w, q_
                        dtype_code(x), x.shape[1], raw_pos0, _ptr(q), dtype_code(q), _ptr(q_idx),
                        dtype_code(q_idx), _ptr(q_idx_scale), _ptr(w), q_pos0, q.shape[1], kv, keys,
                        n_cached, _ptr(out), dtype_code(out))
+
+
+def debug_stall_next(kernel: int):
+    """csa_debug_stall_next: arm the one-shot test aid that makes the next
+    launch of the named tensor-core kernel give up on a wait (0 disarms)."""
+    _check(lib.csa_debug_stall_next(kernel))
 
 
 def device_status(stream=None):

@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -130,11 +131,27 @@ int check_window(const csa_params* p, const csa_rows* raw, int64_t raw_pos0, int
   return CSA_OK;
 }
 
+std::atomic<int> g_stall_next{0};
+
 }  // namespace
+
+namespace csa {
+bool take_debug_stall(int kernel) {
+  int want = kernel;
+  return g_stall_next.compare_exchange_strong(want, 0);
+}
+}  // namespace csa
 
 extern "C" {
 
 const char* csa_last_error(void) { return g_err; }
+
+int csa_debug_stall_next(int kernel) {
+  REQUIRE(kernel == 0 || kernel == CSA_STALL_INDEX || kernel == CSA_STALL_ATTEND,
+          CSA_ERR_INVALID_ARG, "unknown kernel %d", kernel);
+  g_stall_next.store(kernel);
+  return ok();
+}
 
 int csa_device_status(csa_stream_t stream) {
   int code = 0, code2 = 0;

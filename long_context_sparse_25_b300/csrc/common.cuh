@@ -96,6 +96,11 @@ cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dty
                          int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
                          bool fill_invisible = true);
 
+// Test aid (csa_debug_stall_next): true once, for the first launch of the
+// named kernel after the aid was armed, which then clears it.
+enum { kStallIndex = 1, kStallAttend = 2 };
+bool take_debug_stall(int kernel);
+
 // Read and clear the device error words of the bounded waits (0 = none).
 cudaError_t index_tc_status(int* code, cudaStream_t st);
 cudaError_t attend_tc_status(int* code, cudaStream_t st);

@@ -38,6 +38,7 @@ namespace csa {
 namespace {
 
 __device__ int g_index_tc_error = 0;
+__device__ int g_index_never_set = 0;  // the test aid's flag: nothing sets it
 
 constexpr int kTileKeys = 128;
 constexpr int kMaxAcc = 8;  // accumulator buffers in TMEM (up to 512 columns)
@@ -52,6 +53,7 @@ struct TcArgs {
   uint32_t a_bytes, b_bytes, a_chunk_bytes, b_chunk_bytes;
   int chunk_elems, n_chunks, ksteps;
   uint32_t tmem_cols;
+  int stall;  // test aid: CTA 0's MMA issuer first waits on a flag that nothing sets
   const float* w;
   const float* q_scale;  // e4m3 only
   const float* k_scale;  // e4m3 only
@@ -247,6 +249,8 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       uint32_t qcount = 0, bi = 0;
       int pb = -1, pqb = -1;
       bool ok = true;
+      // test aid: the producer's first loads are in flight while this waits
+      if (a.stall && blockIdx.x == 0) ok = tc::flag_wait(&g_index_never_set, tc::kStallNs, err, 7);
       while (ok && sch.next(b, qb, kt)) {
         if (b != pb || qb != pqb) {
           if (qcount > 0) tc::mma_commit(&b_empty[(qcount - 1) % a.nb]);
@@ -538,6 +542,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   a.q_scale = q_scale;
   a.k_scale = keys.scale;
   a.scores = scores;
+  a.stall = take_debug_stall(kStallIndex) ? 1 : 0;
 
   CUtensorMap tm_keys, tm_q;
   if (!make_map(&tm_keys, keys.data, fp8, (int64_t)p.B * keys.n_rows, p.d_I, kTileKeys))

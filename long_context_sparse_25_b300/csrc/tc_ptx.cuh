@@ -85,6 +85,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Wait until *flag != 0.  Gives up after limit_ns, or as soon as another
+// thread has recorded an error, and then returns false (after recording
+// `code` in *err).  Used only by the test aid that makes a kernel wait on a
+// flag that nothing sets (csa_debug_stall_next), to exercise the same
+// give-up, drain and report path as a real wait that runs out.
+__device__ __forceinline__ bool flag_wait(const int* flag, uint64_t limit_ns, int* err, int code) {
+  const uint64_t t0 = globaltimer();
+  while (*reinterpret_cast<const volatile int*>(flag) == 0) {
+    if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      atomicCAS(err, 0, code);
+      return false;
+    }
+    __nanosleep(1000);
+  }
+  return true;
+}
+
+constexpr uint64_t kStallNs = 100000000ull;  // 0.1 s: the test aid's wait
+
 // Bounded wait that ignores errors recorded by other threads: used on the way
 // out to let this CTA's own copies / MMAs in flight land before it exits.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
@@ -196,18 +216,6 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-
-// Four rows of a 2-D tensor (a one-row box each), gathered into 4 consecutive
-// box-sized rows of shared memory; completion counted on `bar`.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
-      "r"(r3)
-      : "memory");
-}
 
 // Make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (tensor-core operand reads).

@@ -49,7 +49,8 @@ __all__ = [
     "decode_bf16", "encode_bf16", "round_to_bf16", "decode_e4m3", "encode_e4m3",
     "round_to_f32", "quantize_rows_e4m3", "dequantize_rows_e4m3", "store_rows",
     "compress_weights", "compress", "n_vis", "index_scores", "topk_row", "topk",
-    "window_range", "attend_keys", "csa_attend", "hca_attend", "csa_pipeline",
+    "window_range", "attend_keys", "csa_attend", "raw_block_tokens", "csa_attend_raw",
+    "hca_attend", "csa_pipeline",
 ]
 
 E4M3_MAX = 448.0
@@ -334,6 +335,37 @@ def csa_attend(q, entries, raw, raw_pos0: int, sel, q_pos, W: int, D_v: int,
         s = s[s >= 0]
         lo, hi = window_range(t, W)
         keys = np.concatenate([entries[s], raw[lo - raw_pos0: hi - raw_pos0]], axis=0)
+        out[i] = attend_keys(q[i], keys, D_v, scale)
+    return out
+
+
+def raw_block_tokens(sel_row, m: int) -> np.ndarray:
+    """Positions of the raw tokens inside the selected blocks, block by block in
+    list order: entry s covers tokens s*m .. s*m+m-1 (-1 slots skipped)."""
+    s = np.asarray(sel_row, dtype=np.int64)
+    s = s[s >= 0]
+    return (s[:, None] * m + np.arange(m, dtype=np.int64)[None, :]).ravel()
+
+
+def csa_attend_raw(q, raw, raw_pos0: int, sel, q_pos, m: int, W: int, D_v: int,
+                   scale: float) -> np.ndarray:
+    """Raw-token variant of the CSA attention for one sequence ([yudong] 2.2
+    Steps 3-4: the top blocks stand for the 4 original tokens each, and the
+    attention runs over those original tokens; [hongke] 2.2, item 3: standard
+    attention over the raw tokens inside the retrieved blocks).
+
+    Keys of query i: the raw rows of the m tokens of every selected block, in
+    list order, followed by the raw window of query i (kept, as in the entry
+    path, without de-duplication).  The value is a key row's first D_v dims.
+    raw [R, D_qk] holds positions raw_pos0 .. raw_pos0+R-1."""
+    q = np.asarray(q, dtype=np.float64)
+    Q, H, _ = q.shape
+    out = np.zeros((Q, H, D_v))
+    for i in range(Q):
+        t = int(q_pos[i])
+        toks = raw_block_tokens(sel[i], m)
+        lo, hi = window_range(t, W)
+        keys = np.concatenate([raw[toks - raw_pos0], raw[lo - raw_pos0: hi - raw_pos0]], axis=0)
         out[i] = attend_keys(q[i], keys, D_v, scale)
     return out
 

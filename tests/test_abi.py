@@ -93,3 +93,11 @@ def test_workspace_query_and_forward_workspace_check():
     a.kv = _rows(64)
     a.keys = _rows(16)
     assert csa.lib.csa_forward(C.byref(p), C.byref(a), FAKE, 16, None) == -4
+
+
+def test_debug_stall_aid_validates_its_argument():
+    """csa_debug_stall_next touches no GPU state: it only arms a one-shot."""
+    from long_context_sparse_25_b300 import csa
+    assert csa.lib.csa_debug_stall_next(99) == -1
+    assert csa.lib.csa_debug_stall_next(-1) == -1
+    assert csa.lib.csa_debug_stall_next(0) == 0

@@ -416,3 +416,60 @@ def test_pipeline_with_a_filled_cache_equals_the_run_without_one():
                           kv_cache=kv_cache, key_cache=key_cache, n_cached=n_cached, **kw)
     for a, b in zip(full, part):
         assert np.array_equal(a, b)
+
+
+# ------------------------------------------------ raw-token variant of the CSA attention
+def test_raw_variant_with_m1_equals_the_entry_path():
+    """m = 1: an entry is its one raw token (compression with m = 1 is the
+    identity), so attending over the raw tokens of the selected blocks is
+    attending over the selected entries."""
+    x, q, D_v = _dense_case(T=30)
+    T = x.shape[0]
+    pos = np.arange(10, T)
+    sel = np.stack([np.concatenate([np.sort(rng.choice(t + 1, size=6, replace=False)), [-1, -1]])
+                    for t in pos])
+    a = O.csa_attend_raw(q[10:], x, 0, sel, pos, 1, 4, D_v, 0.3)
+    b = O.csa_attend(q[10:], x, x, 0, sel, pos, 4, D_v, 0.3)
+    assert np.array_equal(a, b)
+
+
+def test_raw_variant_all_blocks_no_window_is_block_causal_dense_attention():
+    """m = 4, every visible block selected, W = 0: query t attends densely over
+    the raw tokens 0 .. 4*n_vis(t)-1 (the tokens of its complete blocks);
+    checked against torch's scaled_dot_product_attention with that mask."""
+    T, m, H, D, D_v, scale = 26, 4, 3, 9, 5, 0.45
+    x = rng.standard_normal((T, D))
+    q = rng.standard_normal((T, H, D))
+    pos = np.arange(T)
+    nv = (pos + 1) // m
+    sel = np.full((T, T // m), -1)
+    for t in range(T):
+        sel[t, : nv[t]] = rng.permutation(nv[t])  # any order: a set of keys
+    got = O.csa_attend_raw(q, x, 0, sel, pos, m, 0, D_v, scale)
+    mask = np.full((T, T), -np.inf)
+    for t in range(T):
+        mask[t, : nv[t] * m] = 0.0
+    seen = nv > 0
+    ref = _sdpa(q[seen], x, x[:, :D_v], scale, mask=mask[seen])
+    np.testing.assert_allclose(got[seen], ref, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(got[~seen], np.zeros_like(got[~seen]))  # no key: zeros
+
+
+def test_raw_variant_keys_by_absolute_position_with_window():
+    """Raw rows that start at raw_pos0 > 0; the keys of each query are
+    assembled here by absolute position (the 4 tokens of every selected block,
+    then the window) and compared with torch's scaled_dot_product_attention."""
+    T, m, W, H, D, D_v, scale = 64, 4, 5, 2, 8, 6, 0.3
+    x = rng.standard_normal((T, D))
+    pos = np.arange(56, T)
+    q = rng.standard_normal((pos.size, H, D))
+    sel = np.stack([np.sort(rng.choice((t + 1) // m, size=3, replace=False)) for t in pos])
+    r0 = 16  # earliest selectable block below is 4 (tokens 16..19): make it so
+    sel = np.maximum(sel, 4)
+    sel = np.stack([np.unique(r)[:3] if np.unique(r).size >= 3 else np.array([4, 5, 6]) for r in sel])
+    got = O.csa_attend_raw(q, x[r0:], r0, sel, pos, m, W, D_v, scale)
+    for i, t in enumerate(pos):
+        toks = [4 * s + j for s in sel[i] for j in range(4)] + list(range(t - W + 1, t + 1))
+        keys = x[toks]
+        ref = _sdpa(q[i:i + 1], keys, keys[:, :D_v], scale)
+        np.testing.assert_allclose(got[i:i + 1], ref, rtol=1e-12, atol=1e-13)
