@@ -386,9 +386,15 @@ def algorithmic_work(wl):
         w["index_flops"] = float(B * nv.sum() * wl.H_I * wl.d_I * 2)
         # the visible scores read once, the index lists written
         w["topk_bytes"] = B * (nv.sum() * 4 + wl.Q * wl.k * 4)
-        keys = np.minimum(wl.k, nv) + win
+        sel = np.minimum(wl.k, nv)
+        if wl.attend == "raw":  # the m raw tokens of every selected block
+            keys = sel * m + win
+            gathered = sel.sum() * m * wl.D_qk * esz
+        else:
+            keys = sel + win
+            gathered = sel.sum() * entry_b
         w["attend_flops"] = float(B * keys.sum() * wl.H * (wl.D_qk + wl.D_v) * 2)
-        w["attend_bytes"] = B * (np.minimum(wl.k, nv).sum() * entry_b + win.sum() * wl.D_qk * esz
+        w["attend_bytes"] = B * (gathered + win.sum() * wl.D_qk * esz
                                  + wl.Q * wl.H * (wl.D_qk + wl.D_v) * esz)
     else:  # HCA: every visible entry plus the window
         w["compress_bytes"] = B * new * (m * 2 * wl.D_qk * esz + entry_b)
@@ -450,8 +456,11 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
         "index": lambda: csa.index(p, inp["q_idx"], inp["w"], step.keys, wl.q_pos0, N, scores,
                                    q_scale=inp.get("q_idx_scale"), stream=stream),
         "topk": lambda: csa.topk(p, scores, wl.q_pos0, sel, ws=rest, stream=stream),
-        "attend": lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0,
-                                     N, step.out, ws=rest, stream=stream),
+        "attend": (lambda: csa.attend_raw(p, inp["q"], csa.rows(inp["x_all"]), 0, sel, wl.q_pos0,
+                                          N, step.out, ws=rest, stream=stream))
+        if wl.attend == "raw" else
+        (lambda: csa.attend(p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0, N,
+                            step.out, ws=rest, stream=stream)),
     }
     if not parts_wanted:
         parts = {}
@@ -519,7 +528,8 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     def new_inputs(d):
         # What a step brings in: a decode step's new token (its query rows and
         # its raw KV / indexer-key rows with their gates; the earlier raw rows
-        # of the window arrived with earlier steps and stay resident); every
+        # of the window arrived with earlier steps and stay resident, as do the
+        # raw rows of every position that the raw-token attention reads); every
         # input of a prefill step.
         out = []
         for k in keys_in:
@@ -668,7 +678,8 @@ def run_ours(args, wl):
         prefill = secondary("csa_prefill_64k", args.steps)
         if not args.no_others:
             # the other rows of the path: HCA prefill and decode, mixed-precision decode
-            for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k"):
+            for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k",
+                         "csa_decode_raw_1m"):
                 others[name] = secondary(name, min(args.steps, 10))
 
     if rank != 0:

@@ -220,6 +220,28 @@ int csa_attend(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_
                csa_stream_t stream);
 
 /*
+ * csa_attend_raw -- the raw-token variant of the CSA attention ([yudong] 2.2
+ * Steps 3-4: each selected block stands for its m original tokens and the
+ * attention runs over those tokens; hongke120.com page, section 2.2, item 3):
+ *   keys K = { raw token s*m + r : s in idx[b,i,:], s >= 0, r < m }, block by
+ *            block in list order, ++ { raw token u in window(t) }
+ *   out[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . K_j) * K_j[0:D_v]
+ * A window token is a key of its own even when a selected block holds it.
+ *
+ *   q, idx, out, ws  as for csa_attend; ws of at least
+ *             csa_workspace_size(p, CSA_WS_ATTEND_RAW, Q, N) bytes.
+ *   raw       raw-token rows, width D_qk (F32 or BF16), row j = position
+ *             raw_pos0 + j; raw_pos0 must be 0 and the rows must hold every
+ *             token of the N blocks (n_rows >= m*N) and every window.
+ * Errors: as csa_attend, and INVALID_ARG when the raw rows do not start at
+ * position 0 or cannot hold the blocks' tokens.
+ */
+int csa_attend_raw(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_rows* raw,
+                   int64_t raw_pos0, const int32_t* idx, int64_t q_pos0, int Q, int64_t N,
+                   void* out, csa_dtype out_dtype, void* ws, size_t ws_bytes,
+                   csa_stream_t stream);
+
+/*
  * hca_attend -- HCA dense attention ([csdn] section "V4 改进一：CSA 与 HCA",
  * the HCA paragraph; [yudong] 2.3 Step 2): as csa_attend with the key set every visible entry
  * s < min(N, n_vis(t)) (p->m is the HCA block size, e.g. 128; p->k and the
@@ -256,6 +278,14 @@ typedef struct {
   int64_t n_cached;    /* entries already in both caches */
   void* out;           /* [B, Q, H, D_v] */
   csa_dtype out_dtype;
+  /* Raw-token variant (csa_attend_raw): the raw KV rows of positions
+   * 0 .. raw_all_rows-1 of every sequence, [B, raw_all_rows, D_qk] in
+   * raw_dtype, holding every token of the visible blocks and the windows;
+   * the attention then runs over the raw tokens of the selected blocks and
+   * reads its window from here.  NULL: the attention runs over the selected
+   * entries (csa_attend). */
+  const void* raw_all;
+  int64_t raw_all_rows;
 } csa_forward_args;
 
 /*
@@ -264,14 +294,16 @@ typedef struct {
  *      caches from the raw rows (csa_compress);
  *   2. score every visible entry (csa_index);
  *   3. keep the top-k (csa_topk);
- *   4. attend over them plus the window (csa_attend).
+ *   4. attend over them plus the window (csa_attend; csa_attend_raw over the
+ *      raw tokens of the selected blocks when raw_all is given).
  * The scores and index lists live in the workspace:
  *   ws_bytes >= csa_workspace_size(p, CSA_WS_FORWARD, Q, N).
  */
 int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t ws_bytes,
                 csa_stream_t stream);
 
-enum { CSA_WS_TOPK = 0, CSA_WS_ATTEND = 1, CSA_WS_HCA = 2, CSA_WS_FORWARD = 3 };
+enum { CSA_WS_TOPK = 0, CSA_WS_ATTEND = 1, CSA_WS_HCA = 2, CSA_WS_FORWARD = 3,
+       CSA_WS_ATTEND_RAW = 4 };
 
 /* Workspace bytes needed by the call `which` (CSA_WS_*) for Q queries per
  * sequence over N entries; 0 on invalid arguments. */

@@ -19,7 +19,7 @@ LIB_PATH = _PKG / "libcsa_b300.so"
 HEADER = _PKG.parent / "include" / "csa.h"
 
 F32, BF16, E4M3 = 0, 1, 2
-WS_TOPK, WS_ATTEND, WS_HCA, WS_FORWARD = 0, 1, 2, 3
+WS_TOPK, WS_ATTEND, WS_HCA, WS_FORWARD, WS_ATTEND_RAW = 0, 1, 2, 3, 4
 STALL_INDEX, STALL_ATTEND = 1, 2
 STATUS = {0: "CSA_OK", -1: "CSA_ERR_INVALID_ARG", -2: "CSA_ERR_UNSUPPORTED", -3: "CSA_ERR_ALIGNMENT",
           -4: "CSA_ERR_WORKSPACE", -5: "CSA_ERR_CUDA", -6: "CSA_ERR_TIMEOUT"}
@@ -60,7 +60,8 @@ class ForwardArgs(C.Structure):
                 ("q", C.c_void_p), ("q_dtype", C.c_int), ("q_idx", C.c_void_p),
                 ("q_idx_dtype", C.c_int), ("q_idx_scale", C.c_void_p), ("w", C.c_void_p),
                 ("q_pos0", C.c_int64), ("Q", C.c_int), ("kv", Rows), ("keys", Rows),
-                ("n_cached", C.c_int64), ("out", C.c_void_p), ("out_dtype", C.c_int)]
+                ("n_cached", C.c_int64), ("out", C.c_void_p), ("out_dtype", C.c_int),
+                ("raw_all", C.c_void_p), ("raw_all_rows", C.c_int64)]
 
 
 _P, _I, _I64, _SZ = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
@@ -72,6 +73,8 @@ _SIGS = {
                    _I, _I64, _P, _I, _P, _SZ, _P],
     "hca_attend": [C.POINTER(Params), _P, _I, C.POINTER(Rows), C.POINTER(Rows), _I64, _I64, _I,
                    _I64, _P, _I, _P, _SZ, _P],
+    "csa_attend_raw": [C.POINTER(Params), _P, _I, C.POINTER(Rows), _I64, _P, _I64, _I, _I64, _P,
+                       _I, _P, _SZ, _P],
     "csa_forward": [C.POINTER(Params), C.POINTER(ForwardArgs), _P, _SZ, _P],
     "csa_topk_noalloc": [C.POINTER(Params), _P, _I64, _I, _I64, _P, _P],
 }
@@ -194,6 +197,17 @@ def attend(p: Params, q, kv: Rows, raw: Rows | None, raw_pos0, idx, q_pos0, N, o
                           0 if ws is None else ws.numel(), _stream(stream)))
 
 
+def attend_raw(p: Params, q, raw: Rows, raw_pos0, idx, q_pos0, N, out, ws=None, stream=None):
+    """csa_attend_raw: attention over the m raw tokens of every selected block
+    plus the window."""
+    Q = q.shape[1]
+    if ws is None:
+        ws = _workspace(workspace_size(p, WS_ATTEND_RAW, Q, N), q.device)
+    _check(lib.csa_attend_raw(C.byref(p), _ptr(q), dtype_code(q), C.byref(raw), raw_pos0,
+                              _ptr(idx), q_pos0, Q, N, _ptr(out), dtype_code(out), _ptr(ws),
+                              0 if ws is None else ws.numel(), _stream(stream)))
+
+
 def hca(p: Params, q, kv: Rows, raw: Rows | None, raw_pos0, q_pos0, N, out, ws=None, stream=None):
     Q = q.shape[1]
     if ws is None:
@@ -205,11 +219,14 @@ def hca(p: Params, q, kv: Rows, raw: Rows | None, raw_pos0, q_pos0, N, out, ws=N
 
 
 def forward_args(*, x, gate, bias, xi, gate_i, bias_i, raw_pos0, q, q_idx, w, q_pos0, kv: Rows,
-                 keys: Rows, n_cached, out, q_idx_scale=None) -> ForwardArgs:
+                 keys: Rows, n_cached, out, q_idx_scale=None, raw_all=None) -> ForwardArgs:
+    """Arguments of csa_forward.  raw_all (raw rows of every position from 0)
+    selects the raw-token attention."""
     return ForwardArgs(_ptr(x), _ptr(gate), _ptr(bias), _ptr(xi), _ptr(gate_i), _ptr(bias_i),
                        dtype_code(x), x.shape[1], raw_pos0, _ptr(q), dtype_code(q), _ptr(q_idx),
                        dtype_code(q_idx), _ptr(q_idx_scale), _ptr(w), q_pos0, q.shape[1], kv, keys,
-                       n_cached, _ptr(out), dtype_code(out))
+                       n_cached, _ptr(out), dtype_code(out), _ptr(raw_all),
+                       0 if raw_all is None else raw_all.shape[1])
 
 
 def debug_stall_next(kernel: int):

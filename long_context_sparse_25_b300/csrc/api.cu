@@ -286,33 +286,49 @@ extern "C" int csa_topk_noalloc(const csa_params* p, const float* scores, int64_
                      "csa_topk_noalloc");
 }
 
+// The raw rows of the raw-token variant must hold every token a selected
+// block can cover (positions 0 .. m*N-1) besides the windows.
+static int check_raw_blocks(const csa_params* p, const csa_rows* raw, int64_t raw_pos0, int64_t N) {
+  REQUIRE(raw_pos0 == 0, CSA_ERR_INVALID_ARG,
+          "raw-token attention: raw rows must start at position 0 (raw_pos0 = %lld)",
+          (long long)raw_pos0);
+  REQUIRE(raw->n_rows >= N * p->m, CSA_ERR_INVALID_ARG,
+          "raw-token attention: %lld raw rows cannot hold the tokens of %lld blocks of %d",
+          (long long)raw->n_rows, (long long)N, p->m);
+  return CSA_OK;
+}
+
 static int attend_common(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_rows* kv,
-                         const csa_rows* raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                         const csa_rows* raw, int64_t raw_pos0, const int32_t* idx, int mode,
                          int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype, void* ws,
                          size_t ws_bytes, cudaStream_t st, const char* name) {
-  CHECK(check_params(p, false, !dense));
+  CHECK(check_params(p, false, mode != kAttendDense));
   CHECK(check_attn_params(p));
   CHECK(check_positions(q_pos0, Q, N, p->m));
   REQUIRE(q_dtype == CSA_F32 || q_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED, "q must be F32 or BF16");
   REQUIRE(out_dtype == CSA_F32 || out_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
           "out must be F32 or BF16");
-  CHECK(check_rows(kv, "kv", p->D_qk, N, true, p->D_v));
-  if (p->window > 0) {
+  if (mode != kAttendRawBlocks) CHECK(check_rows(kv, "kv", p->D_qk, N, true, p->D_v));
+  if (p->window > 0 || mode == kAttendRawBlocks) {
     CHECK(check_rows(raw, "raw", p->D_qk, 0, false, -1));
     REQUIRE(raw_pos0 >= 0, CSA_ERR_INVALID_ARG, "raw_pos0 < 0");
     CHECK(check_window(p, raw, raw_pos0, q_pos0, Q));
   }
+  if (mode == kAttendRawBlocks) CHECK(check_raw_blocks(p, raw, raw_pos0, N));
   if (Q == 0) return ok();
   CHECK_PTR(q);
   CHECK_PTR(out);
-  if (!dense) CHECK_PTR(idx);
-  const size_t need = attend_workspace(*p, Q, N, dense);
+  if (mode != kAttendDense) CHECK_PTR(idx);
+  const size_t need = attend_workspace(*p, Q, N, mode);
   if (need) {
     REQUIRE(ws && ws_bytes >= need, CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
     REQUIRE(aligned16(ws), CSA_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   }
-  csa_rows raw_or_empty = raw && p->window > 0 ? *raw : *kv;
-  return cuda_status(launch_attend(*p, q, q_dtype, *kv, raw_or_empty, raw_pos0, idx, dense, q_pos0,
+  // the kernels take two row blocks: without raw rows they get the entry cache
+  // twice, without an entry cache (raw-token variant) the raw rows twice
+  const csa_rows& kv_or_raw = mode == kAttendRawBlocks ? *raw : *kv;
+  const csa_rows& raw_or_kv = (raw && (p->window > 0 || mode == kAttendRawBlocks)) ? *raw : *kv;
+  return cuda_status(launch_attend(*p, q, q_dtype, kv_or_raw, raw_or_kv, raw_pos0, idx, mode, q_pos0,
                                    Q, N, out, out_dtype, ws, st),
                      name);
 }
@@ -321,14 +337,22 @@ int csa_attend(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_
                const csa_rows* raw, int64_t raw_pos0, const int32_t* idx, int64_t q_pos0, int Q,
                int64_t N, void* out, csa_dtype out_dtype, void* ws, size_t ws_bytes,
                csa_stream_t stream) {
-  return attend_common(p, q, q_dtype, kv, raw, raw_pos0, idx, false, q_pos0, Q, N, out, out_dtype,
-                       ws, ws_bytes, (cudaStream_t)stream, "csa_attend");
+  return attend_common(p, q, q_dtype, kv, raw, raw_pos0, idx, kAttendEntries, q_pos0, Q, N, out,
+                       out_dtype, ws, ws_bytes, (cudaStream_t)stream, "csa_attend");
+}
+
+int csa_attend_raw(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_rows* raw,
+                   int64_t raw_pos0, const int32_t* idx, int64_t q_pos0, int Q, int64_t N,
+                   void* out, csa_dtype out_dtype, void* ws, size_t ws_bytes,
+                   csa_stream_t stream) {
+  return attend_common(p, q, q_dtype, nullptr, raw, raw_pos0, idx, kAttendRawBlocks, q_pos0, Q, N,
+                       out, out_dtype, ws, ws_bytes, (cudaStream_t)stream, "csa_attend_raw");
 }
 
 int hca_attend(const csa_params* p, const void* q, csa_dtype q_dtype, const csa_rows* kv,
                const csa_rows* raw, int64_t raw_pos0, int64_t q_pos0, int Q, int64_t N, void* out,
                csa_dtype out_dtype, void* ws, size_t ws_bytes, csa_stream_t stream) {
-  return attend_common(p, q, q_dtype, kv, raw, raw_pos0, nullptr, true, q_pos0, Q, N, out,
+  return attend_common(p, q, q_dtype, kv, raw, raw_pos0, nullptr, kAttendDense, q_pos0, Q, N, out,
                        out_dtype, ws, ws_bytes, (cudaStream_t)stream, "hca_attend");
 }
 
@@ -339,12 +363,16 @@ size_t csa_workspace_size(const csa_params* p, int which, int Q, int64_t N) {
   if (!p || Q < 0 || N < 0 || p->B < 1) return 0;
   switch (which) {
     case CSA_WS_TOPK: return topk_workspace(*p, Q, N);
-    case CSA_WS_ATTEND: return attend_workspace(*p, Q, N, false);
-    case CSA_WS_HCA: return attend_workspace(*p, Q, N, true);
+    case CSA_WS_ATTEND: return attend_workspace(*p, Q, N, kAttendEntries);
+    case CSA_WS_HCA: return attend_workspace(*p, Q, N, kAttendDense);
+    case CSA_WS_ATTEND_RAW: return attend_workspace(*p, Q, N, kAttendRawBlocks);
     case CSA_WS_FORWARD: {
+      // either attention of csa_forward (entries, or the raw tokens of the blocks)
       size_t s = align256((size_t)p->B * Q * N * sizeof(float));
       s += align256((size_t)p->B * Q * (size_t)(p->k > 0 ? p->k : 0) * sizeof(int32_t));
-      size_t a = topk_workspace(*p, Q, N), b = attend_workspace(*p, Q, N, false);
+      size_t a = topk_workspace(*p, Q, N), b = attend_workspace(*p, Q, N, kAttendEntries);
+      const size_t c = attend_workspace(*p, Q, N, kAttendRawBlocks);
+      if (c > b) b = c;
       return s + align256(a > b ? a : b);
     }
     default: return 0;
@@ -378,7 +406,20 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
   CHECK(check_rows(&a->kv, "kv", p->D_qk, N, true, p->D_v));
   CHECK(check_rows(&a->keys, "keys", p->d_I, N, true, p->d_I));
   CHECK(check_rows(&raw, "raw", p->D_qk, 0, false, -1));
-  CHECK(check_window(p, &raw, a->raw_pos0, a->q_pos0, a->Q));
+  // raw-token variant: the attention reads every raw row from raw_all
+  csa_rows raw_all = raw;
+  const int mode = a->raw_all ? kAttendRawBlocks : kAttendEntries;
+  if (a->raw_all) {
+    raw_all.data = const_cast<void*>(a->raw_all);
+    raw_all.n_rows = a->raw_all_rows;
+    CHECK(check_rows(&raw_all, "raw_all", p->D_qk, 0, false, -1));
+    REQUIRE(raw_all.dtype == CSA_BF16 || raw_all.dtype == CSA_F32, CSA_ERR_UNSUPPORTED,
+            "raw_all must be F32 or BF16");
+    CHECK(check_window(p, &raw_all, 0, a->q_pos0, a->Q));
+    CHECK(check_raw_blocks(p, &raw_all, 0, N));
+  } else {
+    CHECK(check_window(p, &raw, a->raw_pos0, a->q_pos0, a->Q));
+  }
   if (N > a->n_cached) {
     REQUIRE(a->n_cached * p->m >= a->raw_pos0 && N * p->m <= a->raw_pos0 + a->R, CSA_ERR_INVALID_ARG,
             "entries [%lld, %lld) pool tokens outside the raw rows [%lld, %lld)",
@@ -423,8 +464,12 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/index");
   e = launch_topk(*p, scores, a->q_pos0, a->Q, N, idx, rest, st);
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/topk");
-  e = launch_attend(*p, a->q, a->q_dtype, a->kv, raw, a->raw_pos0, idx, false, a->q_pos0, a->Q, N,
-                    a->out, a->out_dtype, rest, st);
+  if (mode == kAttendRawBlocks)
+    e = launch_attend(*p, a->q, a->q_dtype, raw_all, raw_all, 0, idx, mode, a->q_pos0, a->Q, N,
+                      a->out, a->out_dtype, rest, st);
+  else
+    e = launch_attend(*p, a->q, a->q_dtype, a->kv, raw, a->raw_pos0, idx, mode, a->q_pos0, a->Q, N,
+                      a->out, a->out_dtype, rest, st);
   return cuda_status(e, "csa_forward/attend");
 }
 

@@ -22,10 +22,10 @@
 namespace csa {
 
 bool attend_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& kv,
-                         const csa_rows& raw, int Q, int64_t N, csa_dtype out_dtype);
-size_t attend_tc_workspace(const csa_params& p, int Q, int64_t N, bool dense, int64_t q_pos0);
+                         const csa_rows& raw, int Q, int64_t N, csa_dtype out_dtype, int mode);
+size_t attend_tc_workspace(const csa_params& p, int Q, int64_t N, int mode, int64_t q_pos0);
 cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows& kv,
-                             const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                             const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, int mode,
                              int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
                              void* ws, cudaStream_t st);
 
@@ -36,22 +36,30 @@ constexpr int kKT = 32;       // keys per tile
 constexpr int kThreads = 256;
 constexpr int kMaxDvPerThread = 32;  // D_v <= 512
 
-// Row of the virtual key list: entry index (>= 0), or window token (encoded
-// as -(pos + 2)), or -1 for an empty slot.
+// Row of the virtual key list: entry index (>= 0), or raw token (a window
+// token or a token of a selected block, encoded as -(pos + 2)), or -1 for an
+// empty slot.
 struct KeyList {
   const int32_t* idx;  // [k] selected entries of this query, or nullptr (dense)
-  int k;               // length of the entry part
+  int k;               // length of the first part (entries, or raw tokens of the blocks)
+  int m;               // raw-token blocks: tokens per block; 0 otherwise
+  int64_t N;           // entries in the cache
   int64_t lo;          // first window position
-  int64_t len;         // entry part + window
+  int64_t len;         // first part + window
   __device__ __forceinline__ int64_t at(int64_t j) const {
-    if (j < k) return idx ? (int64_t)idx[j] : j;
+    if (j < k) {
+      if (!idx) return j;
+      if (m == 0) return (int64_t)idx[j];
+      const int64_t s = idx[j / m];
+      return (s >= 0 && s < N) ? -((s * m + j % m) + 2) : -1;
+    }
     return -((lo + (j - k)) + 2);
   }
 };
 
 __global__ void __launch_bounds__(kThreads) attend_simt_kernel(
     const void* __restrict__ q, csa_dtype q_dtype, RowView kv, RowView raw, int64_t raw_pos0,
-    const int32_t* __restrict__ idx, int dense, int64_t q_pos0, int Q, int64_t N, int H,
+    const int32_t* __restrict__ idx, int mode, int64_t q_pos0, int Q, int64_t N, int H,
     int D_qk, int D_v, int k, int W, int m, float scale, int splits, int64_t split_len,
     void* __restrict__ out, csa_dtype out_dtype, float* __restrict__ ws) {
   extern __shared__ float sm[];
@@ -72,12 +80,15 @@ __global__ void __launch_bounds__(kThreads) attend_simt_kernel(
 
   KeyList kl;
   kl.lo = t - W + 1 > 0 ? t - W + 1 : 0;
-  if (dense) {
+  kl.N = N;
+  kl.m = 0;
+  if (mode == kAttendDense) {
     int64_t nv = n_vis(t, m);
     kl.k = (int)(nv < N ? nv : N);
     kl.idx = nullptr;
   } else {
-    kl.k = k;
+    kl.k = mode == kAttendRawBlocks ? k * m : k;
+    kl.m = mode == kAttendRawBlocks ? m : 0;
     kl.idx = idx + qrow * (int64_t)k;
   }
   kl.len = kl.k + (t - kl.lo + 1);
@@ -228,10 +239,12 @@ __global__ void combine_kernel(const float* __restrict__ ws, int splits, int D_v
 
 // Split rule: a fixed number of keys per split, chosen from the key-list
 // length only.  Prefill-sized launches (many queries) use one split.
-void split_plan(const csa_params& p, int Q, int64_t N, bool dense, int* splits, int64_t* split_len) {
+void split_plan(const csa_params& p, int Q, int64_t N, int mode, int* splits, int64_t* split_len) {
   int64_t max_len;
-  if (dense) {
+  if (mode == kAttendDense) {
     max_len = N + p.window;
+  } else if (mode == kAttendRawBlocks) {
+    max_len = (int64_t)p.k * p.m + p.window;
   } else {
     max_len = (int64_t)p.k + p.window;
   }
@@ -253,28 +266,28 @@ void split_plan(const csa_params& p, int Q, int64_t N, bool dense, int* splits, 
 // the larger of the CUDA-core split partials and the tensor-core ones.  The
 // tensor-core plan is largest for the latest query, which sees the most
 // entries, so that position bounds it for every q_pos0.
-size_t attend_workspace(const csa_params& p, int Q, int64_t N, bool dense) {
+size_t attend_workspace(const csa_params& p, int Q, int64_t N, int mode) {
   int splits;
   int64_t split_len;
-  split_plan(p, Q, N, dense, &splits, &split_len);
+  split_plan(p, Q, N, mode, &splits, &split_len);
   size_t simt = 0;
   if (splits > 1) simt = (size_t)p.B * Q * p.H * splits * (p.D_v + 2) * sizeof(float);
-  const size_t tc = attend_tc_workspace(p, Q, N, dense, (int64_t)1 << 62);
+  const size_t tc = attend_tc_workspace(p, Q, N, mode, (int64_t)1 << 62);
   return simt > tc ? simt : tc;
 }
 
 cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype, const csa_rows& kv,
-                          const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                          const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, int mode,
                           int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
                           void* ws, cudaStream_t st) {
   const int64_t rows = (int64_t)p.B * Q;
   if (rows <= 0) return cudaSuccess;
-  if (attend_tc_supported(p, q_dtype, kv, raw, Q, N, out_dtype))
-    return launch_attend_tc(p, q, kv, raw, raw_pos0, idx, dense, q_pos0, Q, N, out, out_dtype, ws,
+  if (attend_tc_supported(p, q_dtype, kv, raw, Q, N, out_dtype, mode))
+    return launch_attend_tc(p, q, kv, raw, raw_pos0, idx, mode, q_pos0, Q, N, out, out_dtype, ws,
                             st);
   int splits;
   int64_t split_len;
-  split_plan(p, Q, N, dense, &splits, &split_len);
+  split_plan(p, Q, N, mode, &splits, &split_len);
   const int D_qk = p.D_qk;
   size_t smem = ((size_t)kHG * D_qk + (size_t)kKT * (D_qk + 1) + kHG * kKT + kHG) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(attend_simt_kernel,
@@ -282,7 +295,7 @@ cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype,
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)rows, (unsigned)ceil_div(p.H, kHG), (unsigned)splits);
   attend_simt_kernel<<<grid, kThreads, smem, st>>>(
-      q, q_dtype, make_view(kv), make_view(raw), raw_pos0, idx, dense ? 1 : 0, q_pos0, Q, N, p.H,
+      q, q_dtype, make_view(kv), make_view(raw), raw_pos0, idx, mode, q_pos0, Q, N, p.H,
       D_qk, p.D_v, p.k, p.window, p.m, p.scale, splits, split_len, out, out_dtype,
       reinterpret_cast<float*>(ws));
   e = cudaGetLastError();

@@ -110,9 +110,14 @@ int topk_launches(const csa_params& p, int Q, int64_t N);
 cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0, int Q, int64_t N,
                         int32_t* idx, void* ws, cudaStream_t st);
 
-size_t attend_workspace(const csa_params& p, int Q, int64_t N, bool dense);
+// Key list of the attention: the selected entries (CSA), every visible
+// entry (HCA), or the m raw tokens of every selected entry's block (the
+// raw-token variant of CSA); the raw window follows in every case.
+enum AttendMode { kAttendEntries = 0, kAttendDense = 1, kAttendRawBlocks = 2 };
+
+size_t attend_workspace(const csa_params& p, int Q, int64_t N, int mode);
 cudaError_t launch_attend(const csa_params& p, const void* q, csa_dtype q_dtype, const csa_rows& kv,
-                          const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, bool dense,
+                          const csa_rows& raw, int64_t raw_pos0, const int32_t* idx, int mode,
                           int64_t q_pos0, int Q, int64_t N, void* out, csa_dtype out_dtype,
                           void* ws, cudaStream_t st);
 

@@ -4,7 +4,8 @@
 workload and runs the whole path with ``run()``:
 
 * CSA prefill / decode: one ``csa_forward`` call (compress the new entries,
-  index, top-k, attend);
+  index, top-k, attend over the selected entries or, for the raw-token
+  workloads, over the raw tokens of the selected blocks);
 * HCA prefill / decode: ``csa_compress`` of the new entries (m' = 128) then
   ``hca_attend``.
 
@@ -56,7 +57,8 @@ class Step:
                 x=inp["x"], gate=inp["g"], bias=inp["bias"], xi=inp["xi"], gate_i=inp["gi"],
                 bias_i=inp["bias_i"], raw_pos0=wl.raw_pos0, q=inp["q"], q_idx=inp["q_idx"],
                 w=inp["w"], q_pos0=wl.q_pos0, kv=self.kv, keys=self.keys,
-                n_cached=self.n_cached, out=self.out, q_idx_scale=inp.get("q_idx_scale"))
+                n_cached=self.n_cached, out=self.out, q_idx_scale=inp.get("q_idx_scale"),
+                raw_all=inp.get("x_all") if wl.attend == "raw" else None)
             nbytes = csa.workspace_size(self.p, csa.WS_FORWARD, wl.Q, N)
         else:
             nbytes = csa.workspace_size(self.p, csa.WS_HCA, wl.Q, N)
@@ -85,6 +87,8 @@ class Step:
         tc = wl.dtype != "f32" and wl.H == 128
         if wl.mode.startswith("hca"):
             kd = min((wl.q_pos0 + wl.Q) // wl.m, wl.N)
+        elif wl.attend == "raw":
+            kd = wl.k * wl.m
         else:
             kd = wl.k
         n_keys = ((kd + 3) // 4) * 4 + wl.W

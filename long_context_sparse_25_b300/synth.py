@@ -21,6 +21,10 @@ Workloads (sizes from the pages' configurations):
 * ``csa_decode_fp8_512k`` -- mixed-precision CSA decode, B=64, context
   524,288: nope dims e4m3 + per-entry fp32 scale, rope dims bf16; indexer keys
   and queries e4m3 with per-row scales; 1% of values x20.
+* ``csa_decode_raw_1m`` -- the CSA decode step of ``csa_decode_1m`` with the
+  raw-token attention: the raw KV rows of all 2^20 positions are resident
+  (``x_all``), and each query attends over the 4 raw tokens of each of its
+  1024 selected blocks plus the window.
 """
 
 from __future__ import annotations
@@ -56,6 +60,7 @@ class Workload:
     outliers: float = 0.0   # probability that an element is multiplied by 20
     q_std: float = 1.0      # extra factor on Q (the tiny case folds 1/sqrt(128))
     softmax_scale: float | None = None
+    attend: str = "entries"  # "entries" | "raw": the raw tokens of the selected blocks
 
     @property
     def N(self) -> int:
@@ -104,6 +109,9 @@ WORKLOADS = {
     "csa_decode_fp8_512k": Workload("csa_decode_fp8_512k", "csa_decode", B=64, L=1 << 19, m=4,
                                     H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128,
                                     Q=1, dtype="mixed", seed=4, outliers=0.01),
+    "csa_decode_raw_1m": Workload("csa_decode_raw_1m", "csa_decode", B=32, L=1 << 20, m=4, H=128,
+                                  D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
+                                  dtype="bf16", seed=2, attend="raw"),
 }
 
 # tensor ids (the generator of tensor `name` is seeded with seed * 1000 + id)
@@ -118,12 +126,14 @@ def _gen(wl: Workload, name: str, device) -> torch.Generator:
     return g
 
 
-def _normal(wl, name, shape, device, std=1.0, rms=False, outl=None, chunk_rows=1 << 16):
-    """float32 N(0, std^2) tensor, optionally RMSNorm'd per last-dim row and with
-    outliers; drawn in row chunks of a fixed size so that memory stays bounded."""
+def _normal(wl, name, shape, device, std=1.0, rms=False, outl=None, chunk_rows=1 << 16,
+            out_dtype=torch.float32):
+    """N(0, std^2) tensor, optionally RMSNorm'd per last-dim row and with
+    outliers, drawn in float32 in row chunks of a fixed size (so that memory
+    stays bounded) and stored in out_dtype (round to nearest even)."""
     gen = _gen(wl, name, device)
     gen_o = _gen(wl, outl, device) if (outl is not None and wl.outliers > 0) else None
-    out = torch.empty(shape, dtype=torch.float32, device=device)
+    out = torch.empty(shape, dtype=out_dtype, device=device)
     flat = out.view(-1, shape[-1])
     for r0 in range(0, flat.shape[0], chunk_rows):
         r1 = min(flat.shape[0], r0 + chunk_rows)
@@ -171,8 +181,17 @@ def make_inputs(wl: Workload, device="cpu") -> dict:
     """
     B, R = wl.B, wl.raw_rows
     rows_dtype = "f32" if wl.dtype == "f32" else "bf16"
+    tdt = torch.float32 if rows_dtype == "f32" else torch.bfloat16
     inp = {}
-    inp["x"] = _store(_normal(wl, "x", (B, R, wl.D_qk), device, rms=wl.rmsnorm), rows_dtype)
+    if wl.attend == "raw" and R < wl.L:
+        # the raw-token attention reads raw rows of every position: all L rows
+        # are drawn, and the step's own rows are their last R
+        inp["x_all"] = _normal(wl, "x", (B, wl.L, wl.D_qk), device, rms=wl.rmsnorm, out_dtype=tdt)
+        inp["x"] = inp["x_all"][:, wl.L - R:].contiguous()
+    else:
+        inp["x"] = _store(_normal(wl, "x", (B, R, wl.D_qk), device, rms=wl.rmsnorm), rows_dtype)
+        if wl.attend == "raw":
+            inp["x_all"] = inp["x"]
     inp["g"] = _store(_normal(wl, "g", (B, R, wl.D_qk), device), rows_dtype)
     inp["bias"] = _normal(wl, "bias", (wl.m, wl.D_qk), device, std=0.1)
     inp["q"] = _store(_normal(wl, "q", (B, wl.Q, wl.H, wl.D_qk), device, std=wl.q_std,

@@ -87,6 +87,8 @@ class SeqOracle:
                 self.q_idx = f64(qi)
             self.w = f64(inp["w"][b])
         self.q = f64(inp["q"][b])
+        # raw-token attention: the raw rows of every position from 0
+        self.raw_all = f64(inp["x_all"][b]) if wl.attend == "raw" else None
 
     def positions(self, qs):
         return self.wl.q_pos0 + np.asarray(qs)
@@ -96,6 +98,9 @@ class SeqOracle:
 
     def attend(self, qs, sel):
         wl = self.wl
+        if wl.attend == "raw":
+            return O.csa_attend_raw(self.q[qs], self.raw_all, 0, sel, self.positions(qs), wl.m,
+                                    wl.W, wl.D_v, wl.scale)
         return O.csa_attend(self.q[qs], self.kv, self.raw, wl.raw_pos0, sel, self.positions(qs),
                             wl.W, wl.D_v, wl.scale)
 
@@ -171,3 +176,19 @@ def check_out(gpu: np.ndarray, ref: np.ndarray, f32: bool, unit_scale: bool = Tr
     else:
         assert fro <= FRO_BF16 and mx <= MAXABS_BF16, f"fro {fro:.3e}, max-abs error {mx:.3e}"
     return fro, mx
+
+
+class DeviceRows:
+    """Rows of one sequence's raw-token tensor, fetched from the device on
+    demand and decoded exactly to float64: the oracle indexes its raw rows by
+    position (an index array or a slice), and the full-size raw rows (2^20
+    positions) are too large to decode whole on the host."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, key):
+        if isinstance(key, slice):
+            return f64(self.t[key])
+        idx = torch.as_tensor(np.asarray(key), device=self.t.device).long()
+        return f64(self.t[idx])

@@ -16,7 +16,7 @@ import oracle as O
 from long_context_sparse_25_b300 import csa, synth
 from long_context_sparse_25_b300.pipeline import Step
 
-from harness import check_out, check_scores, check_selection, f64
+from harness import DeviceRows, check_out, check_scores, check_selection, f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -55,7 +55,11 @@ def _decode_parity(wl, dev, attn_seqs):
         ref = O.index_scores(qi, f64(inp["w"][b]), keys, pos, m)
         check_scores(step.scores()[b].cpu().double().numpy(), ref)
         check_selection(sel_all[b], ref, O.n_vis(pos, m), wl.k)
-        if b in attn_seqs:
+        if b in attn_seqs and wl.attend == "raw":
+            o = O.csa_attend_raw(f64(inp["q"][b]), DeviceRows(inp["x_all"][b]), 0, sel_all[b],
+                                 pos, m, wl.W, wl.D_v, wl.scale)
+            check_out(out[b], o, False)
+        elif b in attn_seqs:
             s = sel_all[b, 0]
             s = s[s >= 0]
             rows = torch.from_numpy(s).to(dev).long()
@@ -75,6 +79,16 @@ def _decode_parity(wl, dev, attn_seqs):
 
 def test_decode_1m_full_size(cuda_device):
     wl = synth.WORKLOADS["csa_decode_1m"]
+    _decode_parity(wl, cuda_device, attn_seqs={0, 5, 11, 16, 21, 26, 30, 31})
+
+
+def test_decode_raw_1m_full_size(cuda_device):
+    """The raw-token attention at the headline decode size (B = 32, 2^20
+    positions, the raw KV rows of every position resident): per query the
+    4 raw tokens of each of the 1024 selected blocks plus the 128-token window
+    (4,224 keys, 33 tiles, split runs with the combine); scores and selection
+    as for the entry path, attention on a fixed sample of 8 sequences."""
+    wl = synth.WORKLOADS["csa_decode_raw_1m"]
     _decode_parity(wl, cuda_device, attn_seqs={0, 5, 11, 16, 21, 26, 30, 31})
 
 

@@ -70,3 +70,25 @@ def test_disarmed_aid_changes_nothing(cuda_device):
     torch.cuda.synchronize()
     csa.device_status()
     assert torch.equal(step.out, out)
+
+
+def test_attention_wait_that_runs_out_is_reported_and_the_context_recovers(cuda_device):
+    """The same for the tensor-core attention: the stalled launch's first CTA
+    has its first gathers in flight; the report names the attention's site."""
+    wl = synth.WORKLOADS["csa_decode_1m"].replace(B=2, L=20000)
+    inp = synth.make_inputs(wl, cuda_device)
+    step = Step(wl, inp)
+    step.run()
+    torch.cuda.synchronize()
+    csa.device_status()
+    want = step.out.clone()
+    sel = step.selected()
+    csa.debug_stall_next(csa.STALL_ATTEND)
+    csa.attend(step.p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0, wl.N, step.out)
+    with pytest.raises(csa.CsaError) as e:
+        csa.device_status()
+    assert e.value.code == -6 and "site 28" in str(e.value), str(e.value)
+    csa.attend(step.p, inp["q"], step.kv, step.raw, wl.raw_pos0, sel, wl.q_pos0, wl.N, step.out)
+    torch.cuda.synchronize()
+    csa.device_status()
+    assert torch.equal(step.out, want)
