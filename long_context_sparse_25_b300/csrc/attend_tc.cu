@@ -36,10 +36,9 @@
 //
 // Gathers.  Three producer warps fill the ring: each lane gathers 16-byte
 // units of its rows with cp.async, which arrive on the chunk's barrier by
-// themselves once they land.  A tile of 128 consecutive valid entries (HCA),
-// a tile of window rows, or a tile of raw-token blocks (m = 4 consecutive
-// rows each) is loaded by TMA boxes instead, issued by one thread that
-// accounts for every producer's arrival.  For every tile the producers issue
+// themselves once they land.  A tile of 128 consecutive valid entries (HCA)
+// or of window rows is one TMA box per chunk instead, issued by one thread
+// that accounts for every producer's arrival.  For every tile the producers issue
 // the D_qk/64 key chunks of that tile, then the D_v/128 value chunks of the
 // previous tile (the ring is too small to keep them from the score pass).
 //
@@ -318,18 +317,12 @@ __device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(count)
                : "memory");
 }
-// A 64-column x 4-row TMA box (one raw-token block) into 4 swizzled rows.
-__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                              int x, int y) {
-  tc::tma_load_2d(dst, map, bar, x, y);
-}
 
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv,
-                     const __grid_constant__ CUtensorMap tm_raw,
-                     const __grid_constant__ CUtensorMap tm_raw4, const AttArgs a) {
+                     const __grid_constant__ CUtensorMap tm_raw, const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -381,7 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!kE4M3) {
       if (a.mode == kDense) tc::prefetch_tmap(&tm_kv);
       if (a.W > 0) tc::prefetch_tmap(&tm_raw);
-      if (a.mode == kRawBlocks) tc::prefetch_tmap(&tm_raw4);
     }
   }
   if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, 512);
@@ -397,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's barrier by themselves when they land, so a producer never waits
     // for its own copies and runs ahead as far as the ring lets it.  A chunk
     // loaded by TMA is issued by warp 0 (lane 0 arrives for all 96 producers,
-    // with the byte count); warps 1-2 skip it.
+    // with the byte count); warps 1-2 only wait for its slot.
     const int pt = threadIdx.x;
     uint32_t pslot = 0, pph = 0;  // ring slot and the parity of its release
     bool ok = true;
@@ -428,8 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t wb;
       SlotSrc s0, s1;
       int tma;    // bf16: 1 = 128 consecutive entry rows, 2 = 128 consecutive raw rows
-      int tma_y;  //   (one box per chunk from tma_y), 3 = 32 raw-token blocks of 4 rows
-      int blk_y;  //   (warp 0 lane L: the raw row of block L); 0 = gathered
+      int tma_y;  //   (one box per chunk from tma_y); 0 = gathered
     };
     auto wait_slot = [&](uint32_t s, uint32_t par) -> bool {
       int okw = 1;
@@ -446,8 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a chunk of codes, or of a value half) into the next ring slot
     auto issue_chunk = [&](int c, const TileRows& t) -> bool {
       if (!kE4M3 && t.tma) {
+        // every warp waits for the slot, also those that do not fill it: a
+        // parity wait cannot tell a release from the one two fills later, so
+        // no warp may run more than one fill of a slot ahead of the consumer
+        if (!wait_slot(pslot, pph)) return false;
         if (warp == 0) {
-          if (!wait_slot(pslot, pph)) return false;
           uint8_t* dst = sRing + pslot * kChunk;
           if (lane == 0) {
             tc::mbar_expect_tx(&ring_full[pslot], kChunk);
@@ -455,12 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_mask |= 1u << pslot;
             tma_par = (tma_par & ~(1u << pslot)) | (pph << pslot);
           }
-          __syncwarp();
-          if (t.tma == 3) {
-            tma_load_rows(dst + lane * 512, &tm_raw4, &ring_full[pslot], c * 64, t.blk_y);
-          } else if (lane == 0) {
+          if (lane == 0)
             tc::tma_load_2d(dst, t.tma == 1 ? &tm_kv : &tm_raw, &ring_full[pslot], c * 64, t.tma_y);
-          }
         }
         advance();
         return true;
@@ -540,10 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A warp's units of a chunk cover 44 key rows (unit i of lane L is row
     // 4 warp + 12 i + L/8, shared by 8 lanes): lane L looks up rows q = L
     // and q = L + 32 of that list and the lanes exchange them by shuffles.
-    // Key-list words are fetched a tile ahead: those two rows, the two mask
-    // slots pt and pt + 96, and (raw-token blocks) block L of the tile.
+    // Key-list words are fetched a tile ahead: those two rows and the two
+    // mask slots pt and pt + 96.
     struct TileWords {
-      int32_t w[5];
+      int32_t w[4];
     };
     const bool has1 = pt + kProd < kT;
     auto unit_row = [&](int q) -> int { return 4 * warp + 12 * (q >> 2) + (q & 3); };
@@ -557,7 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       t.w[1] = (has_q2 && r2 < kT) ? slot_word(a, kl, it.qrow, jt + r2) : 0;
       t.w[2] = slot_word(a, kl, it.qrow, jt + pt);
       t.w[3] = slot_word(a, kl, it.qrow, jt + (has1 ? pt + kProd : pt));
-      t.w[4] = (a.mode == kRawBlocks && warp == 0) ? slot_word(a, kl, it.qrow, jt + lane * a.m) : 0;
     };
     auto tile_rows = [&](const Item& it, int u, const TileWords& tw, TileRows& t) {
       const KeyList& kl = it.kl;
@@ -588,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       t.tma = 0;
       t.tma_y = 0;
-      t.blk_y = 0;
       if (!kE4M3) {
         if (a.mode == kDense && jt + kT <= kl.kd) {
           // every slot a valid entry, entry j in row j (a tile with masked
@@ -601,13 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // window: masked; past the rows: zero-filled)
           t.tma = 2;
           t.tma_y = (int)((int64_t)b * a.raw_rows + (kl.lo - a.raw_pos0) + (jt - kl.k_ent));
-        } else if (a.mode == kRawBlocks && a.m == 4 && jt + kT <= kl.k_ent) {
-          // 32 blocks of 4 consecutive raw rows; an empty slot's block is the
-          // sequence's first 4 rows (valid data, masked in the softmax)
-          t.tma = 3;
-          const int32_t s = tw.w[4];
-          const bool v = s >= 0 && s < a.N;
-          t.blk_y = (int)((int64_t)b * a.raw_rows + (v ? (int64_t)s * 4 - a.raw_pos0 : 0));
         }
       }
       t.s0 = slot_src(a, kl, b, jt + pt, tw.w[2]);
@@ -1219,22 +1200,17 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
                                   ((rows * p.D_v * sizeof(float) + 255) & ~(size_t)255));
 
-  CUtensorMap tm_q, tm_kv, tm_raw, tm_raw4;
+  CUtensorMap tm_q, tm_kv, tm_raw;
   memset(&tm_kv, 0, sizeof(tm_kv));
   memset(&tm_raw, 0, sizeof(tm_raw));
-  memset(&tm_raw4, 0, sizeof(tm_raw4));
   if (!make_map_bf16(&tm_q, q, (int64_t)p.B * Q * p.H, p.D_qk, 128)) return cudaErrorInvalidValue;
   if (!e4m3) {
-    // dense runs of entry rows and window rows load as 128-row boxes, the
-    // raw-token blocks as 4-row boxes
+    // dense runs of entry rows and window rows load as 128-row boxes
     if (mode == kDense &&
         !make_map_bf16(&tm_kv, kv.data, (int64_t)p.B * kv.n_rows, p.D_qk, 128))
       return cudaErrorInvalidValue;
     if (p.window > 0 &&
         !make_map_bf16(&tm_raw, raw.data, (int64_t)p.B * raw.n_rows, p.D_qk, 128))
-      return cudaErrorInvalidValue;
-    if (mode == kRawBlocks && p.m == 4 &&
-        !make_map_bf16(&tm_raw4, raw.data, (int64_t)p.B * raw.n_rows, p.D_qk, 4))
       return cudaErrorInvalidValue;
   }
   int64_t grid = num_sms();
@@ -1248,13 +1224,12 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, tm_raw4, a);
+    attend_tc_kernel<true><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
   } else {
     e = cudaFuncSetAttribute(attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, tm_raw4,
-                                                                    a);
+    attend_tc_kernel<false><<<(unsigned)grid, kThreads, smem, st>>>(tm_q, tm_kv, tm_raw, a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;

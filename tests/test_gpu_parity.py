@@ -31,7 +31,7 @@ CSA_CASES = {
     # fewer): the tensor-core indexer's causal schedule with one query per block
     "decode_bf16_q2": (W["csa_decode_1m"].replace(B=2, L=20000, Q=2), None),
     # raw-token attention (the 4 raw tokens of every selected block, then the
-    # window): decode over 5000 entries, and an 8K prefill (4-row TMA boxes)
+    # window): decode over 5000 entries, and an 8K prefill
     "decode_raw": (W["csa_decode_raw_1m"].replace(B=3, L=20000), None),
     "prefill_raw_8k": (W["csa_prefill_64k"].replace(L=8192, Q=8192, attend="raw"), 24),
     # raw-token attention through the CUDA-core path (fp32)
