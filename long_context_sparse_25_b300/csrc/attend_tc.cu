@@ -22,8 +22,8 @@
 // all 512 TMEM columns, so a work item owns one half of the value dims (256
 // columns) and computes the 128 x 128 score tile S = Q K^T itself.  TMEM: two
 // S buffers (columns 0-255) and O (columns 256-511).  After the softmax reads
-// S it writes P (bf16 pairs) over the first 64 columns of the same buffer,
-// and P . V takes A from TMEM.
+// S it writes P (bf16 pairs) over the score columns it has read, and P . V
+// takes A from TMEM.
 //
 // Persistent CTAs.  A launch enumerates work items (query row, value half,
 // split of the key list); each CTA takes a contiguous range of them and runs
@@ -47,7 +47,8 @@
 // the RoPE dims divided by the row scale (split exactly into a bf16 high and
 // low part, two ring slots that meet the same Q chunk), so the tile holds
 // S'_j = q_nope . code_j + q_rope . (rope_j / c_j) and the softmax takes
-// S_j = c_j S'_j.  P . V runs on the codes with c_j folded into P.
+// S_j = c_j S'_j.  P . V runs on the codes with c_j folded into P, split
+// exactly into a bf16 high and low part (two MMAs per K step).
 //
 // Softmax: one thread per head row, log2 domain, running maximum raised only
 // when a tile's maximum exceeds it by more than 2^8 (then O and the running
@@ -723,9 +724,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t o_tmem = tmem + 256 + 64 * c;
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks) {
-            // 16 keys per K step: 16 rows of 128 bytes
+            // 16 keys per K step: 16 rows of 128 bytes; their P (bf16 pairs)
+            // in 8 columns at 32 (ks/2) + 8 (ks%2), the low part 16 further
             const uint64_t bd = vd + (uint64_t)(ks * (2048 >> 4));
-            tc::mma_bf16_ts(o_tmem, p_tmem + 8 * ks, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
+            const uint32_t pa = p_tmem + 32 * (ks >> 1) + 8 * (ks & 1);
+            tc::mma_bf16_ts(o_tmem, pa, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
+            if (kE4M3) tc::mma_bf16_ts(o_tmem, pa + 16, bd, id_pv, 1u);
           }
           tc::mma_commit(&ring_empty[slot]);
           next_slot();
@@ -827,9 +831,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         // Two passes over the tile's scores, 32 columns at a time (few live
-        // registers): the row maximum, then P.  P (bf16 pairs) of columns
-        // 32q .. 32q+31 goes to columns 16q .. 16q+15 of the buffer, which
-        // pass 2 has already read by then.
+        // registers): the row maximum, then P.  P of keys 32q .. 32q+31 goes,
+        // as bf16 pairs, over the 32 score columns just read: the high part
+        // to columns 32q .. 32q+15, the low part (mixed caches) to 32q+16 ..
+        // 32q+31.
         const uint32_t s_col = tmem + lane_base + sb * 128;
         float m_tile = -INFINITY;
 #pragma unroll 1
@@ -871,17 +876,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
           m_ref = m_tile;
         }
-        // P = 2^(x - m_ref) (mixed caches: times the value row's scale)
+        // P = 2^(x - m_ref) (mixed caches: times the value row's scale,
+        // split exactly into bf16 high + low parts: outlier rows carry values
+        // up to ~20x unit scale, too large for one rounding of P)
 #pragma unroll 1
         for (int gq = 0; gq < kT / 32; ++gq) {
           uint32_t r[32];
           tc::tmem_ld32(s_col + gq * 32, r);
           tc::tmem_wait_ld();
           const uint32_t bw = bal[gq];
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            float pp[2];
+            float pp[2], lo[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int jj = 2 * c + e, j = gq * 32 + jj;
@@ -891,10 +898,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float pj = m_ref == -INFINITY ? 0.f : exp2f(xv - m_ref);
               l_run += pj;
               pp[e] = kE4M3 ? pj * sv : pj;
+              lo[e] = kE4M3 ? pp[e] - __bfloat162float(__float2bfloat16_rn(pp[e])) : 0.f;
             }
             pk[c] = pack_bf16(pp[0], pp[1]);
+            pl[c] = pack_bf16(lo[0], lo[1]);
           }
-          tc::tmem_st16(s_col + gq * 16, pk);
+          tc::tmem_st16(s_col + gq * 32, pk);
+          if (kE4M3) tc::tmem_st16(s_col + gq * 32 + 16, pl);
         }
         tc::tmem_wait_st();
         tc::tc_fence_before();
