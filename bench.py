@@ -429,6 +429,8 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
 
     inp = synth.make_inputs(wl, dev)
     step = Step(wl, inp)
+    # the inputs were drawn on the default stream; the step runs on its own
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
     p = step.p
     N = wl.N

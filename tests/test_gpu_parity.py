@@ -125,8 +125,11 @@ def test_topk_bit_exact_on_oracle_scores(cuda_device):
     """csa_topk fed fp32 scores (with many exact ties, signed zeros, -inf
     beyond visibility) returns exactly the oracle's index lists."""
     rng = np.random.default_rng(5)
+    # rows held in registers (N <= 16384; N % 4 != 0 takes scalar loads), long
+    # rows over several CTAs, rows shorter than k, and a row of all-equal scores
     for (B, Q, N, k, m, q_pos0) in [(2, 37, 700, 64, 4, 2700), (1, 5, 20000, 1024, 4, 79999),
-                                     (3, 9, 300, 1024, 4, 1000), (1, 300, 16384, 1024, 4, 65235)]:
+                                     (3, 9, 300, 1024, 4, 1000), (1, 300, 16384, 1024, 4, 65235),
+                                     (2, 7, 1001, 256, 4, 3998)]:
         s = rng.standard_normal((B, Q, N))
         s = np.where(rng.uniform(size=s.shape) < 0.3, np.round(s, 1), s)  # ties
         s = np.where(rng.uniform(size=s.shape) < 0.05, 0.0, s)
