@@ -36,6 +36,11 @@ Readings where the pages are silent:
   * compressed entries are stored in the cache dtype (fp32 / bf16, or the
     mixed e4m3 + bf16 layout) before anything reads them.
 
+  * the grouped output projection splits the H heads into G consecutive
+    groups of H/G heads; group g's head outputs, concatenated head by head,
+    are projected by its own matrix to d_g features, and the G results are
+    concatenated in group order.
+
 Nothing here is blocked, fused or reordered beyond what the steps state.
 """
 
@@ -50,7 +55,7 @@ __all__ = [
     "round_to_f32", "quantize_rows_e4m3", "dequantize_rows_e4m3", "store_rows",
     "compress_weights", "compress", "n_vis", "index_scores", "topk_row", "topk",
     "window_range", "attend_keys", "csa_attend", "raw_block_tokens", "csa_attend_raw",
-    "hca_attend", "csa_pipeline",
+    "hca_attend", "csa_pipeline", "group_output_projection",
 ]
 
 E4M3_MAX = 448.0
@@ -416,3 +421,28 @@ def csa_pipeline(*, x, g, bias, xi, gi, bias_i, q, q_idx, w, m, k, W, D_v, scale
     sel = topk(scores, q_pos, m, k)
     out = csa_attend(q, entries, x, raw_pos0, sel, q_pos, W, D_v, scale)
     return out, sel, scores
+
+
+# ---------------------------------------------------------------------------
+# Grouped output projection after the shared-KV MQA
+# ---------------------------------------------------------------------------
+
+def group_output_projection(o: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """[csdn] section "V4 改进一：CSA 与 HCA", the CSA paragraph's last
+    sentence: the attention output is projected in groups to save compute.
+
+    o [T, H, D_v] attention outputs; W [G, (H/G)*D_v, d_g], one matrix per
+    group.  Group g holds heads g*H/G .. (g+1)*H/G - 1; its input row is those
+    heads' outputs concatenated head by head, and its d_g outputs fill columns
+    g*d_g .. (g+1)*d_g - 1 of the result [T, G*d_g]."""
+    o = np.asarray(o, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    T, H, D_v = o.shape
+    G, K, d_g = W.shape
+    assert H % G == 0 and K == (H // G) * D_v, (o.shape, W.shape)
+    hg = H // G
+    y = np.zeros((T, G * d_g))
+    for g in range(G):
+        x_g = o[:, g * hg:(g + 1) * hg, :].reshape(T, K)
+        y[:, g * d_g:(g + 1) * d_g] = x_g @ W[g]
+    return y

@@ -473,3 +473,52 @@ def test_raw_variant_keys_by_absolute_position_with_window():
         keys = x[toks]
         ref = _sdpa(q[i:i + 1], keys, keys[:, :D_v], scale)
         np.testing.assert_allclose(got[i:i + 1], ref, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------- grouped output projection
+def test_group_projection_brute_force_indices():
+    """Every output element by an explicit sum over (head, dim) with the
+    group's row index written out: pins the head-to-group assignment and the
+    head-major concatenation inside a group."""
+    T, H, D_v, G, d_g = 3, 6, 4, 3, 5
+    o = rng.standard_normal((T, H, D_v))
+    W = rng.standard_normal((G, (H // G) * D_v, d_g))
+    y = O.group_output_projection(o, W)
+    hg = H // G
+    for t in range(T):
+        for g in range(G):
+            for n in range(d_g):
+                acc = 0.0
+                for h in range(g * hg, (g + 1) * hg):
+                    for d in range(D_v):
+                        acc += o[t, h, d] * W[g, (h - g * hg) * D_v + d, n]
+                assert abs(y[t, g * d_g + n] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_group_projection_is_the_block_diagonal_full_projection():
+    """The grouped projection equals one projection of the flattened output
+    [T, H*D_v] by the block-diagonal matrix of the group matrices (a matrix
+    built with scipy, multiplied with numpy)."""
+    from scipy.linalg import block_diag
+    T, H, D_v, G, d_g = 7, 8, 16, 4, 12
+    o = rng.standard_normal((T, H, D_v))
+    W = rng.standard_normal((G, (H // G) * D_v, d_g))
+    full = o.reshape(T, H * D_v) @ block_diag(*W)
+    np.testing.assert_allclose(O.group_output_projection(o, W), full, rtol=1e-12, atol=1e-12)
+
+
+def test_group_projection_one_group_is_a_plain_matmul_and_groups_are_local():
+    T, H, D_v, d_g = 5, 4, 8, 6
+    o = rng.standard_normal((T, H, D_v))
+    W1 = rng.standard_normal((1, H * D_v, d_g))
+    np.testing.assert_allclose(O.group_output_projection(o, W1),
+                               np.matmul(o.reshape(T, -1), W1[0]), rtol=1e-12, atol=1e-12)
+    # changing the heads of group 1 changes only group 1's columns
+    G = 2
+    W = rng.standard_normal((G, (H // G) * D_v, d_g))
+    y0 = O.group_output_projection(o, W)
+    o2 = o.copy()
+    o2[:, 2:4, :] += 1.0
+    y1 = O.group_output_projection(o2, W)
+    assert np.array_equal(y0[:, :d_g], y1[:, :d_g])
+    assert not np.allclose(y0[:, d_g:], y1[:, d_g:])
