@@ -30,6 +30,12 @@ output read back, the copies overlapped with the neighbouring steps.  Every
 line carries ``cpu_baseline``: the oracle timed on a bounded sample of the
 same workload on the host cores.
 
+``others`` holds the other rows of the path, each with its own roofline,
+e2e and CPU baseline: HCA prefill and decode, the mixed-precision decode,
+the raw-token decode, and ``hybrid_decode_1m``: a CSA layer and an HCA layer
+decoding 128 consecutive tokens of 32 sequences at the end of a 2^20
+context, block compression included at the tokens that complete a block.
+
 With --gpus N > 1 (torchrun, one process per GPU) every rank runs its own
 batch (replicas, weak scaling; no collective on the data path) and the time
 is the max over ranks.
@@ -642,6 +648,232 @@ def roofline(wl, per_part, ms_step, peaks, peak_kind):
     return r
 
 
+def _hybrid_token(hw, t):
+    """The single-layer workloads of one hybrid token at position t: the CSA
+    layer's decode step and the HCA layer's, each over the entries visible
+    at t (the compress part counts only when t completes a block)."""
+    lc = hw.layer("csa").replace(L=t + 1)
+    lh = hw.layer("hca").replace(L=t + 1)
+    return lc, lh
+
+
+def hybrid_work(hw):
+    """Algorithmic bytes and launches of the hybrid run's hw.steps tokens, from
+    the single-layer definitions: per token, the CSA layer's index, top-k and
+    attention and the HCA layer's attention; the compression of a block only
+    at the token that completes it."""
+    tot, launches = 0.0, 0
+    for t in range(hw.t0, hw.t0 + hw.steps):
+        lc, lh = _hybrid_token(hw, t)
+        wc, wh = algorithmic_work(lc), algorithmic_work(lh)
+        tot += wc["index_bytes"] + wc["topk_bytes"] + wc["attend_bytes"] + wh["hca_bytes"]
+        n_keys = (hw.k + 3) // 4 * 4 + hw.W
+        # launch plan (as in the single-layer steps): indexer; top-k (three
+        # kernels for few long rows); tensor-core attention plus a combine
+        # when a decode query's keys exceed 5 tiles of 128
+        launches += 1 + (3 if (lc.N > 16384 and hw.k <= 4096 and hw.B < 256) else 1)
+        launches += 1 + (1 if -(-n_keys // 128) > 5 else 0)
+        nh = lh.N + hw.W
+        launches += 1 + (1 if -(-nh // 128) > 5 else 0)
+        if (t + 1) % hw.m == 0:
+            tot += wc["compress_bytes"]
+            launches += 1  # both caches in one launch
+        if (t + 1) % hw.m1 == 0:
+            tot += wh["compress_bytes"]
+            launches += 1
+    return tot, launches
+
+
+def measure_hybrid(args, hw, dev, peaks, peak_kind, reps):
+    """Hybrid decoding: a CSA layer and an HCA layer decode hw.steps
+    consecutive tokens of B sequences.  The run of hw.steps tokens is one CUDA
+    graph, replayed `reps` times (the decoder rewinds to t0 between replays;
+    every replay recomputes the same cache entries from the same rows); e2e
+    runs the decoder's own per-token calls eagerly with each token's rows and
+    queries copied from pinned host memory and both outputs read back."""
+    from long_context_sparse_25_b300 import csa, hybrid, synth
+
+    inp = synth.make_hybrid_inputs(hw, dev)
+    pc = csa.params(hw.B, hw.m, hw.H, hw.D_qk, hw.D_v, hw.H_I, hw.d_I, hw.k, hw.W, hw.scale)
+    ph = csa.params(hw.B, hw.m1, hw.H, hw.D_qk, hw.D_v, 0, 0, 0, hw.W, hw.scale)
+    t0, S = hw.t0, hw.steps
+    dec = hybrid.HybridDecoder(pc, ph, t0=t0, max_len=t0 + S, device=dev, bias0=inp["bias0"],
+                               bias_i0=inp["bias_i0"], bias1=inp["bias1"],
+                               raw_rows=hw.raw_rows, held=hw.held)
+    n, n1 = t0 // hw.m, t0 // hw.m1
+    dec.kv[:, :n].copy_(inp.pop("kv"))
+    dec.keys[:, :n].copy_(inp.pop("keys"))
+    dec.ent[:, :n1].copy_(inp.pop("ent"))
+    held = t0 - dec.p0
+    assert dec.p0 == hw.p0 and held + S <= hw.raw_rows, "the run must fit the raw buffers"
+    for name in hybrid.RAW_NAMES:
+        # the rows already held, and every decoded token's rows written ahead
+        dec.raw[name][:, :held + S].copy_(inp[name])
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+
+    def run_all():
+        dec.rewind(t0)
+        for s in range(S):
+            dec.step(inp["q0"][s], inp["q_idx0"][s], inp["w0"][s], inp["q1"][s], stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_all()
+    torch.cuda.synchronize()
+    csa.device_status(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run_all()
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // 2)):
+            g.replay()
+    torch.cuda.synchronize()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a_.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    csa.device_status(stream)
+    ms_tok = a_.elapsed_time(b_) / (reps * S)
+    tot_bytes, launches = hybrid_work(hw)
+    ach = tot_bytes / S / (ms_tok / 1e3) / 1e9
+
+    # end to end through the decoder's calls: per token, its six raw rows and
+    # four query tensors from pinned host memory, both outputs back
+    names_q = ("q0", "q_idx0", "w0", "q1")
+    host_rows = {k: inp[k][:, held:held + S].transpose(0, 1).unsqueeze(2).cpu().contiguous()
+                 .pin_memory() for k in hybrid.RAW_NAMES}  # [S, B, 1, w]
+    host_q = {k: inp[k].cpu().pin_memory() for k in names_q}
+    dq = {k: torch.empty_like(inp[k][0]) for k in names_q}
+    out_h = [torch.empty(dec.out0.shape, dtype=dec.out0.dtype, pin_memory=True),
+             torch.empty(dec.out1.shape, dtype=dec.out1.dtype, pin_memory=True)]
+    bi = sum(v[0].numel() * v.element_size() for v in host_rows.values()) + \
+        sum(v[0].numel() * v.element_size() for v in host_q.values())
+    bo = sum(o.numel() * o.element_size() for o in out_h)
+
+    def e2e_run():
+        dec.rewind(t0)
+        for s in range(S):
+            with torch.cuda.stream(stream):
+                for k in hybrid.RAW_NAMES:
+                    dec.slot(k).copy_(host_rows[k][s], non_blocking=True)
+                for k in names_q:
+                    dq[k].copy_(host_q[k][s], non_blocking=True)
+                o0, o1 = dec.step(dq["q0"], dq["q_idx0"], dq["w0"], dq["q1"], stream=stream)
+                out_h[0].copy_(o0, non_blocking=True)
+                out_h[1].copy_(o1, non_blocking=True)
+
+    e2e_run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    csa.device_status(stream)
+    e2e_ms = e0.elapsed_time(e1) / S
+    # leave the decoder's state as the graph left it (the raw rows of the
+    # decoded tokens were rewritten with the same values)
+    row = {
+        "workload": (f"{hw.name}: a CSA layer (k={hw.k}, indexer {hw.H_I}x{hw.d_I}) and an HCA "
+                     f"layer (m'={hw.m1}), H={hw.H}, D={hw.D_v}+{hw.D_qk - hw.D_v}, window "
+                     f"{hw.W}, B={hw.B}, {S} consecutive tokens at positions {t0}..{t0 + S - 1} "
+                     f"(context 2^20, one 128-token block completed), bf16"),
+        "value": hw.B / (ms_tok / 1e3), "unit": "tok/s", "ms_per_token": ms_tok,
+        "steps": reps * S,
+        "timing": f"one CUDA graph of the {S} tokens, replayed {reps} times; CUDA events",
+        "roofline": {"bound": "hbm", "algorithmic_bytes_per_token": tot_bytes / S,
+                     "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} HBM copy"},
+        "e2e": {"value": hw.B / (e2e_ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo,
+                "note": "eager per-token calls (host launch cost included), copies on the "
+                        "compute stream"},
+        "gpu_launches": launches * reps,
+    }
+    del dec, inp, g, host_rows, host_q
+    gc.collect()
+    torch.cuda.empty_cache()
+    return row
+
+
+def measure_gproj(args, gw, dev, peaks, peak_kind, steps):
+    """The grouped output projection (csa_group_proj) of one attention output:
+    a CUDA graph of one call, CUDA events; e2e copies o from pinned host
+    memory and reads y back every step."""
+    from long_context_sparse_25_b300 import csa, synth
+
+    inp = synth.make_gproj_inputs(gw, dev)
+    y = torch.empty((gw.T, gw.G * gw.d_g), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    f = lambda: csa.group_proj(inp["o"], inp["w"], y, stream=stream)
+    with torch.cuda.stream(stream):
+        f()
+    torch.cuda.synchronize()
+    csa.device_status(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        f()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a_.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    csa.device_status(stream)
+    ms = a_.elapsed_time(b_) / steps
+    flops = 2.0 * gw.T * gw.G * gw.K * gw.d_g
+    nbytes = (gw.T * gw.H * gw.D_v + gw.G * gw.d_g * gw.K + gw.T * gw.G * gw.d_g) * 2.0
+    decode = gw.T < 1024
+    if decode:  # the weights stream from HBM
+        ach = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": nbytes,
+                "peak_kind": f"{peak_kind} HBM copy"}
+    else:
+        ach = flops / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                "frac_sustained": ach / peaks["bf16_tflops_sustained"],
+                "frac_nominal": ach / NOMINAL_BF16_TFLOPS, "algorithmic_flops_per_launch": flops,
+                "peak_kind": f"{peak_kind} bf16 burst"}
+    # end to end: o in from pinned host memory, y back
+    host_o = inp["o"].cpu().pin_memory()
+    host_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    ne = 2 if not decode else steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(ne):
+            inp["o"].copy_(host_o, non_blocking=True)
+            g.replay()
+            host_y.copy_(y, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / ne
+    unit = "tok/s" if decode else "query-tok/s"
+    row = {"workload": (f"{gw.name}: grouped output projection of a [{gw.T}, {gw.H}, {gw.D_v}] "
+                        f"attention output, {gw.G} groups of {gw.H // gw.G} heads -> {gw.d_g} "
+                        f"features each (K = {gw.K}), bf16"),
+           "value": gw.T / (ms / 1e3), "unit": unit, "ms_per_step": ms, "steps": steps,
+           "roofline": roof,
+           "e2e": {"value": gw.T / (e2e_ms / 1e3), "unit": unit,
+                   "h2d_bytes_per_step": host_o.numel() * 2, "d2h_bytes_per_step": host_y.numel() * 2},
+           "gpu_launches": steps}
+    del inp, y, g, host_o, host_y
+    gc.collect()
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_ours(args, wl):
     from long_context_sparse_25_b300 import synth
 
@@ -683,6 +915,13 @@ def run_ours(args, wl):
             for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k",
                          "csa_decode_raw_1m"):
                 others[name] = secondary(name, min(args.steps, 10))
+            # a CSA layer and an HCA layer decoding token by token
+            others["hybrid_decode_1m"] = measure_hybrid(args, synth.HYBRID["hybrid_decode_1m"],
+                                                        dev, peaks, peak_kind, reps=3)
+            # the grouped output projection after the attention
+            for name in ("gproj_prefill_64k", "gproj_decode_b32"):
+                others[name] = measure_gproj(args, synth.GPROJ[name], dev, peaks, peak_kind,
+                                             steps=min(args.steps, 10))
 
     if rank != 0:
         if dist:
@@ -729,6 +968,21 @@ def main():
                     help="override the workload's context length (a prefill keeps every query)")
     args = ap.parse_args()
     from long_context_sparse_25_b300 import synth
+    if args.workload in synth.GPROJ and args.impl == "ours":
+        torch.cuda.set_device(0)
+        peaks, peak_kind = _peaks()
+        row = measure_gproj(args, synth.GPROJ[args.workload], torch.device("cuda", 0), peaks,
+                            peak_kind, steps=args.steps)
+        print(json.dumps(row), flush=True)
+        return
+    if args.workload in synth.HYBRID and args.impl == "ours":
+        # the hybrid decode row alone
+        torch.cuda.set_device(0)
+        peaks, peak_kind = _peaks()
+        row = measure_hybrid(args, synth.HYBRID[args.workload], torch.device("cuda", 0), peaks,
+                             peak_kind, reps=max(1, args.steps // 5))
+        print(json.dumps(row), flush=True)
+        return
     wl = synth.WORKLOADS[args.workload]
     if args.batch:
         wl = wl.replace(B=args.batch)

@@ -337,6 +337,28 @@ int csa_device_status(csa_stream_t stream);
 enum { CSA_STALL_INDEX = 1, CSA_STALL_ATTEND = 2 };
 int csa_debug_stall_next(int kernel);
 
+/*
+ * csa_group_proj -- grouped output projection after the attention ([csdn]
+ * section "V4 改进一：CSA 与 HCA", the CSA paragraph's last sentence: the
+ * output is projected in groups to save compute).  The H heads form G
+ * consecutive groups of H/G heads; group g's head outputs, side by side in a
+ * row of o, are projected by that group's own matrix:
+ *   y[t, g*d_g + n] = sum_{j < K} o[t, g*K + j] * w[g, n, j],   K = (H/G)*D_v
+ *
+ *   o   [T, H, D_v] BF16 (the attention output, e.g. csa_attend's `out` with
+ *       T = B*Q), row-major, caller-owned device memory.
+ *   w   [G, d_g, K] BF16: row n of group g holds column n of the group's
+ *       [K, d_g] matrix (both operands K-contiguous).
+ *   y   [T, G*d_g], dtype y_dtype (F32 or BF16; fp32 accumulation, one
+ *       rounding at the end), written completely.
+ * Runs on the tensor cores; needs K a multiple of 64 and d_g a multiple of
+ * 256 (else CSA_ERR_UNSUPPORTED), H a multiple of G (CSA_ERR_INVALID_ARG),
+ * o / w / y 16-byte aligned (CSA_ERR_ALIGNMENT).  T = 0 does nothing.  Its
+ * bounded device waits report through csa_device_status.
+ */
+int csa_group_proj(const void* o, int64_t T, int H, int D_v, const void* w, int G, int d_g,
+                   void* y, csa_dtype y_dtype, csa_stream_t stream);
+
 /* Message describing the last error returned on the calling thread ("" if none). */
 const char* csa_last_error(void);
 

@@ -77,6 +77,7 @@ _SIGS = {
                        _I, _P, _SZ, _P],
     "csa_forward": [C.POINTER(Params), C.POINTER(ForwardArgs), _P, _SZ, _P],
     "csa_topk_noalloc": [C.POINTER(Params), _P, _I64, _I, _I64, _P, _P],
+    "csa_group_proj": [_P, _I64, _I, _I, _P, _I, _I, _P, _I, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -227,6 +228,16 @@ def forward_args(*, x, gate, bias, xi, gate_i, bias_i, raw_pos0, q, q_idx, w, q_
                        dtype_code(q_idx), _ptr(q_idx_scale), _ptr(w), q_pos0, q.shape[1], kv, keys,
                        n_cached, _ptr(out), dtype_code(out), _ptr(raw_all),
                        0 if raw_all is None else raw_all.shape[1])
+
+
+def group_proj(o, w, y, stream=None):
+    """csa_group_proj: y [.., G*d_g] = the grouped projection of the attention
+    output o [.., H, D_v] with w [G, d_g, (H/G)*D_v]."""
+    H, D_v = o.shape[-2], o.shape[-1]
+    T = o.numel() // (H * D_v) if o.numel() else 0
+    G, d_g = w.shape[0], w.shape[1]
+    _check(lib.csa_group_proj(_ptr(o), T, H, D_v, _ptr(w), G, d_g, _ptr(y), dtype_code(y),
+                              _stream(stream)))
 
 
 def debug_stall_next(kernel: int):

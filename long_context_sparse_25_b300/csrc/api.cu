@@ -160,6 +160,9 @@ int csa_device_status(csa_stream_t stream) {
   e = attend_tc_status(&code2, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "csa_device_status");
   if (code == 0) code = code2;
+  e = gproj_status(&code2, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "csa_device_status");
+  if (code == 0) code = code2;
   if (code != 0)
     return fail(CSA_ERR_TIMEOUT, "a bounded device-side wait gave up (site %d); the outputs of the "
                                  "calls since the last check are not valid", code);
@@ -474,3 +477,25 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
 }
 
 }  // extern "C"
+
+extern "C" int csa_group_proj(const void* o, int64_t T, int H, int D_v, const void* w, int G,
+                              int d_g, void* y, csa_dtype y_dtype, csa_stream_t stream) {
+  REQUIRE(T >= 0 && H >= 1 && D_v >= 1 && G >= 1 && d_g >= 1, CSA_ERR_INVALID_ARG,
+          "bad sizes T=%lld H=%d D_v=%d G=%d d_g=%d", (long long)T, H, D_v, G, d_g);
+  REQUIRE(H % G == 0, CSA_ERR_INVALID_ARG, "H = %d is not a multiple of G = %d", H, G);
+  REQUIRE(y_dtype == CSA_F32 || y_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED, "y must be F32 or BF16");
+  const int64_t K = (int64_t)(H / G) * D_v;
+  REQUIRE(K % 64 == 0 && K <= (1 << 30), CSA_ERR_UNSUPPORTED,
+          "group width (H/G)*D_v = %lld is not a multiple of 64", (long long)K);
+  REQUIRE(d_g % 256 == 0, CSA_ERR_UNSUPPORTED, "d_g = %d is not a multiple of 256", d_g);
+  REQUIRE(T < (1ll << 31) && (int64_t)G * d_g < (1ll << 31), CSA_ERR_UNSUPPORTED, "sizes too large");
+  if (T == 0) return ok();
+  CHECK_PTR(o);
+  CHECK_PTR(w);
+  CHECK_PTR(y);
+  REQUIRE(aligned16(o) && aligned16(w) && aligned16(y), CSA_ERR_ALIGNMENT,
+          "o, w and y must be 16-byte aligned");
+  return cuda_status(launch_group_proj(o, T, H, D_v, w, G, d_g, y, y_dtype == CSA_F32,
+                                       (cudaStream_t)stream),
+                     "csa_group_proj");
+}

@@ -104,6 +104,12 @@ bool take_debug_stall(int kernel);
 // Read and clear the device error words of the bounded waits (0 = none).
 cudaError_t index_tc_status(int* code, cudaStream_t st);
 cudaError_t attend_tc_status(int* code, cudaStream_t st);
+cudaError_t gproj_status(int* code, cudaStream_t st);
+
+// Grouped output projection (gproj_tc.cu): y [T, G*d_g] = per group g,
+// o[:, g*K .. (g+1)*K) . w[g]^T with K = (H/G)*D_v.
+cudaError_t launch_group_proj(const void* o, int64_t T, int H, int D_v, const void* w, int G,
+                              int d_g, void* y, bool y_f32, cudaStream_t st);
 
 size_t topk_workspace(const csa_params& p, int Q, int64_t N);
 int topk_launches(const csa_params& p, int Q, int64_t N);

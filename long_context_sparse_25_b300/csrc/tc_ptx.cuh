@@ -1,7 +1,7 @@
 // Inline-PTX wrappers for the sm_100-family tensor-core path: mbarriers, TMA
 // tile loads, tcgen05 MMA / TMEM.  Written from the PTX ISA's descriptions of
-// these instructions; every wait is bounded (globaltimer) and reports a
-// timeout through an error word instead of spinning forever.
+// these instructions; every wait is bounded and reports a timeout through an
+// error word instead of spinning forever.
 #pragma once
 
 #include <cuda.h>
@@ -10,7 +10,13 @@
 namespace csa {
 namespace tc {
 
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+// A wait gives up once both 2 s of %globaltimer and 2e9 cycles of this SM's
+// clock (1 s at the maximum SM clock) have passed since it began: either
+// counter alone would do, but %globaltimer may step when the driver
+// resynchronises it, and a step must not end a wait that has only just
+// begun.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr long long kWaitTimeoutCycles = 2000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -21,6 +27,19 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Start and expiry test of a bounded wait (see kWaitTimeoutNs).
+struct WaitClock {
+  uint64_t t0;
+  long long c0;
+  __device__ __forceinline__ void start() {
+    t0 = globaltimer();
+    c0 = clock64();
+  }
+  __device__ __forceinline__ bool expired() const {
+    return globaltimer() - t0 > kWaitTimeoutNs && clock64() - c0 > kWaitTimeoutCycles;
+  }
+};
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -72,13 +91,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // then returns false (after recording `code` in *err).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  WaitClock wc;
+  wc.start();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (wc.expired()) {
       atomicCAS(err, 0, code);
       return false;
     }
@@ -108,9 +128,10 @@ constexpr uint64_t kStallNs = 100000000ull;  // 0.1 s: the test aid's wait
 // Bounded wait that ignores errors recorded by other threads: used on the way
 // out to let this CTA's own copies / MMAs in flight land before it exits.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
+  WaitClock wc;
+  wc.start();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if (wc.expired()) return false;
   return true;
 }
 

@@ -25,12 +25,21 @@ Workloads (sizes from the pages' configurations):
   raw-token attention: the raw KV rows of all 2^20 positions are resident
   (``x_all``), and each query attends over the 4 raw tokens of each of its
   1024 selected blocks plus the window.
+* ``gproj_prefill_64k`` / ``gproj_decode_b32`` (``GPROJ``) -- the grouped
+  output projection of the attention output of a 65,536-token prefill and of
+  a 32-sequence decode step: 128 heads x 512 in 8 groups of 16 heads, each
+  group projected to 1,024 features; o ~ N(0, 1), weights ~ N(0, 1/K).
+* ``hybrid_decode_1m`` (``HYBRID``) -- a CSA layer and an HCA layer decoding
+  128 consecutive tokens of B=32 sequences at the end of a 2^20 context (the
+  last token completes a 128-token block), caches drawn like the decode
+  workloads' and raw rows drawn for the positions the sliding buffers hold.
 """
 
 from __future__ import annotations
 
 import dataclasses
 import math
+import types
 from dataclasses import dataclass
 
 import torch
@@ -117,7 +126,8 @@ WORKLOADS = {
 # tensor ids (the generator of tensor `name` is seeded with seed * 1000 + id)
 _IDS = {"x": 1, "g": 2, "bias": 3, "xi": 4, "gi": 5, "bias_i": 6, "q": 7, "q_idx": 8,
         "w": 9, "kv": 10, "keys": 11, "outl_kv": 12, "outl_keys": 13, "outl_q_idx": 14,
-        "outl_x": 15, "outl_q": 16}
+        "outl_x": 15, "outl_q": 16, "x1": 17, "g1": 18, "bias1": 19, "q1": 20, "ent": 21,
+        "o": 22, "wproj": 23}
 
 
 def _gen(wl: Workload, name: str, device) -> torch.Generator:
@@ -232,3 +242,143 @@ def make_inputs(wl: Workload, device="cpu") -> dict:
 def small(wl: Workload, **kw) -> Workload:
     """A reduced copy of a workload (same recipe and dtypes, smaller sizes)."""
     return wl.replace(**kw)
+
+
+# ---------------------------------------------------------------------------
+# Hybrid decoding: a CSA layer and an HCA layer, token by token
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class HybridWorkload:
+    name: str
+    B: int
+    t0: int          # position of the first decoded token
+    steps: int       # tokens decoded
+    H: int
+    D_qk: int
+    D_v: int
+    H_I: int
+    d_I: int
+    k: int
+    W: int
+    seed: int
+    m: int = 4       # CSA block
+    m1: int = 128    # HCA block
+    raw_rows: int = 512
+    held: int | None = None  # raw rows before t0 in the buffers (None: what the first step needs)
+    history: bool = False    # draw the raw rows of every position; the caches are then
+                             # compressed from them (else drawn like the decode workloads')
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D_qk)
+
+    @property
+    def need(self) -> int:
+        return self.W + self.m1
+
+    @property
+    def p0(self) -> int:
+        """First position whose raw rows are drawn."""
+        if self.history:
+            return 0
+        return max(0, self.t0 - (self.held or self.need))
+
+    def layer(self, which: str) -> Workload:
+        """The single-layer workload whose recipe (and seed) the layer's
+        tensors follow."""
+        if which == "csa":
+            return Workload(self.name + ":csa", "csa_decode", self.B, self.t0 + self.steps, self.m,
+                            self.H, self.D_qk, self.D_v, self.H_I, self.d_I, self.k, self.W, 1,
+                            "bf16", self.seed)
+        return Workload(self.name + ":hca", "hca_decode", self.B, self.t0 + self.steps, self.m1,
+                        self.H, self.D_qk, self.D_v, 0, 0, 0, self.W, 1, "bf16", self.seed)
+
+    def replace(self, **kw) -> "HybridWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+HYBRID = {
+    "hybrid_decode_1m": HybridWorkload("hybrid_decode_1m", B=32, t0=(1 << 20) - 128, steps=128,
+                                       H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128,
+                                       seed=5),
+}
+
+
+def make_hybrid_inputs(hw: HybridWorkload, device="cpu") -> dict:
+    """Inputs of a hybrid decode run as torch tensors on ``device`` (bf16 rows,
+    fp32 biases and weights).
+
+    Raw rows of positions p0 .. t0+steps-1 ([B, rows, width]): x0, g0, xi0,
+    gi0 (CSA layer: KV rows, gates, indexer-key rows, gates) and x1, g1 (HCA
+    layer).  Biases bias0 [m, D_qk], bias_i0 [m, d_I], bias1 [m', D_qk].  Per
+    decoded token s: q0[s] [B, 1, H, D_qk], q_idx0[s] [B, 1, H_I, d_I],
+    w0[s] [B, 1, H_I], q1[s] [B, 1, H, D_qk] (stacked on a leading steps
+    axis).  Without ``history``, also the caches before t0: kv [B, t0//m,
+    D_qk], keys [B, t0//m, d_I], ent [B, t0//m', D_qk]."""
+    lc, lh = hw.layer("csa"), hw.layer("hca")
+    B, S = hw.B, hw.steps
+    rows = hw.t0 + S - hw.p0
+    bf = torch.bfloat16
+    inp = {
+        "x0": _normal(lc, "x", (B, rows, hw.D_qk), device, rms=True, out_dtype=bf),
+        "g0": _normal(lc, "g", (B, rows, hw.D_qk), device, out_dtype=bf),
+        "xi0": _normal(lc, "xi", (B, rows, hw.d_I), device, rms=True, out_dtype=bf),
+        "gi0": _normal(lc, "gi", (B, rows, hw.d_I), device, out_dtype=bf),
+        "x1": _normal(lh, "x1", (B, rows, hw.D_qk), device, rms=True, out_dtype=bf),
+        "g1": _normal(lh, "g1", (B, rows, hw.D_qk), device, out_dtype=bf),
+        "bias0": _normal(lc, "bias", (hw.m, hw.D_qk), device, std=0.1),
+        "bias_i0": _normal(lc, "bias_i", (hw.m, hw.d_I), device, std=0.1),
+        "bias1": _normal(lh, "bias1", (hw.m1, hw.D_qk), device, std=0.1),
+        "q0": _normal(lc, "q", (S, B, 1, hw.H, hw.D_qk), device, rms=True, out_dtype=bf),
+        "q_idx0": _normal(lc, "q_idx", (S, B, 1, hw.H_I, hw.d_I), device, rms=True,
+                          out_dtype=bf),
+        "w0": _uniform(lc, "w", (S, B, 1, hw.H_I), device),
+        "q1": _normal(lh, "q1", (S, B, 1, hw.H, hw.D_qk), device, rms=True, out_dtype=bf),
+    }
+    if not hw.history:
+        n, n1 = hw.t0 // hw.m, hw.t0 // hw.m1
+        inp["kv"] = _normal(lc, "kv", (B, n, hw.D_qk), device, rms=True, out_dtype=bf)
+        inp["keys"] = _normal(lc, "keys", (B, n, hw.d_I), device, rms=True, out_dtype=bf)
+        inp["ent"] = _normal(lh, "ent", (B, n1, hw.D_qk), device, rms=True, out_dtype=bf)
+    return inp
+
+
+# ---------------------------------------------------------------------------
+# Grouped output projection
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class GprojWorkload:
+    name: str
+    T: int      # rows of the attention output (tokens)
+    H: int
+    D_v: int
+    G: int      # groups of H/G heads
+    d_g: int    # features per group
+    seed: int
+
+    @property
+    def K(self) -> int:
+        return self.H // self.G * self.D_v
+
+    def replace(self, **kw) -> "GprojWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+GPROJ = {
+    "gproj_prefill_64k": GprojWorkload("gproj_prefill_64k", T=65536, H=128, D_v=512, G=8,
+                                       d_g=1024, seed=6),
+    "gproj_decode_b32": GprojWorkload("gproj_decode_b32", T=32, H=128, D_v=512, G=8, d_g=1024,
+                                      seed=6),
+}
+
+
+def make_gproj_inputs(gw: GprojWorkload, device="cpu") -> dict:
+    """o [T, H, D_v] bf16 ~ N(0, 1); w [G, d_g, K] bf16 ~ N(0, 1/K) (row n of
+    group g = column n of that group's projection matrix)."""
+    seed = types.SimpleNamespace(seed=gw.seed, outliers=0.0)
+    o = _normal(seed, "o", (gw.T, gw.H, gw.D_v), device, out_dtype=torch.bfloat16)
+    w = _normal(seed, "wproj", (gw.G, gw.d_g, gw.K), device, std=1.0 / math.sqrt(gw.K),
+                out_dtype=torch.bfloat16)
+    return {"o": o, "w": w}

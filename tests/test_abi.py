@@ -101,3 +101,18 @@ def test_debug_stall_aid_validates_its_argument():
     assert csa.lib.csa_debug_stall_next(99) == -1
     assert csa.lib.csa_debug_stall_next(-1) == -1
     assert csa.lib.csa_debug_stall_next(0) == 0
+
+
+def test_group_proj_rejects_bad_arguments():
+    f = csa.lib.csa_group_proj
+    # o [T=10, H=128, D_v=512], w [G=8, d_g=256, 8192], y [10, 2048]
+    assert f(FAKE, 10, 128, 512, FAKE, 3, 256, FAKE, csa.BF16, None) == -1  # H % G
+    assert "multiple of G" in csa.lib.csa_last_error().decode()
+    assert f(FAKE, 10, 128, 512, FAKE, 8, 200, FAKE, csa.BF16, None) == -2  # d_g % 256
+    assert f(FAKE, 10, 8, 12, FAKE, 8, 256, FAKE, csa.BF16, None) == -2     # K = 12
+    assert f(FAKE, 10, 128, 512, FAKE, 8, 256, FAKE, csa.E4M3, None) == -2  # y dtype
+    assert f(None, 10, 128, 512, FAKE, 8, 256, FAKE, csa.BF16, None) == -1
+    assert f(FAKE + 8, 10, 128, 512, FAKE, 8, 256, FAKE, csa.BF16, None) == -3
+    assert f(FAKE, -1, 128, 512, FAKE, 8, 256, FAKE, csa.BF16, None) == -1
+    # T = 0: nothing to do, no pointer needed, no launch
+    assert f(None, 0, 128, 512, None, 8, 256, None, csa.BF16, None) == 0
