@@ -53,7 +53,8 @@ import numpy as np
 __all__ = [
     "decode_bf16", "encode_bf16", "round_to_bf16", "decode_e4m3", "encode_e4m3",
     "round_to_f32", "quantize_rows_e4m3", "dequantize_rows_e4m3", "store_rows",
-    "compress_weights", "compress", "n_vis", "index_scores", "topk_row", "topk",
+    "compress_weights", "compress", "n_vis", "index_scores", "index_scores_bf16", "topk_row",
+    "topk",
     "window_range", "attend_keys", "csa_attend", "raw_block_tokens", "csa_attend_raw",
     "hca_attend", "csa_pipeline", "group_output_projection",
 ]
@@ -260,6 +261,16 @@ def index_scores(q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray,
     scores = np.einsum("qj,qjn->qn", w, np.maximum(dots, 0.0))
     vis = np.arange(N)[None, :] < n_vis(np.asarray(q_pos), m)[:, None]
     return np.where(vis, scores, -np.inf)
+
+
+def index_scores_bf16(q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray,
+                      q_pos: np.ndarray, m: int) -> np.ndarray:
+    """The indexer scores stored in bf16 ([csdn] section "V4 的其他升级": the
+    index scores drop to BF16, which doubles the speed of the top-k
+    selection): each score of index_scores rounded to the nearest bf16 value
+    (ties to even); invisible entries stay -inf.  The top-k then runs on these
+    values, ties (now frequent) going to the lower index as before."""
+    return round_to_bf16(index_scores(q_idx, w, keys, q_pos, m))
 
 
 # ---------------------------------------------------------------------------

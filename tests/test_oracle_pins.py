@@ -522,3 +522,34 @@ def test_group_projection_one_group_is_a_plain_matmul_and_groups_are_local():
     y1 = O.group_output_projection(o2, W)
     assert np.array_equal(y0[:, :d_g], y1[:, :d_g])
     assert not np.allclose(y0[:, d_g:], y1[:, d_g:])
+
+
+# ------------------------------------------------------- bf16 index scores
+def test_bf16_index_scores_are_torch_rounded_scores_and_ties_go_low():
+    """The bf16 scores equal torch's bf16 cast of the float64 scores (cast
+    through float32, exact here: the scores are sums of few products of
+    small dyadic values), -inf stays -inf, and the top-k over them breaks the
+    many bf16 ties by the lower index."""
+    Q, H_I, d_I, N, m, k = 3, 4, 8, 600, 4, 37
+    q = rng.integers(-3, 4, (Q, H_I, d_I)) / 4.0
+    keys = rng.integers(-3, 4, (N, d_I)) / 8.0
+    w = rng.integers(1, 5, (Q, H_I)) / 4.0
+    pos = np.array([m * N - 1, 1000, 3])
+    s64 = O.index_scores(q, w, keys, pos, m)
+    s16 = O.index_scores_bf16(q, w, keys, pos, m)
+    ref = torch.from_numpy(s64).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(s16, ref)
+    assert np.array_equal(np.isneginf(s16), np.isneginf(s64))
+    sel = O.topk(s16, pos, m, k)
+    for i in range(Q):
+        nv = int(min(O.n_vis(pos[i], m), N))
+        kk = min(k, nv)
+        order = np.lexsort((np.arange(nv), -s16[i, :nv]))  # score desc, then index asc
+        assert np.array_equal(sel[i, :kk], np.sort(order[:kk]))
+    # a tie group straddling the k-th place keeps only its lowest index
+    vals, counts = np.unique(s16[0, :N], return_counts=True)
+    tie = vals[counts > 1][-1]
+    k2 = int(np.count_nonzero(s16[0, :N] > tie)) + 1
+    sel2 = O.topk(s16[:1], pos[:1], m, k2)[0]
+    group = np.flatnonzero(s16[0, :N] == tie)
+    assert group[0] in sel2 and not np.isin(group[1:], sel2).any()
