@@ -390,8 +390,9 @@ def algorithmic_work(wl):
         w["compress_bytes"] = B * new * (m * 2 * (wl.D_qk + wl.d_I) * esz + entry_b + key_b)
         w["index_bytes"] = B * (N * key_b + wl.Q * (qi_b + wl.H_I * 4))
         w["index_flops"] = float(B * nv.sum() * wl.H_I * wl.d_I * 2)
-        # the visible scores read once, the index lists written
-        w["topk_bytes"] = B * (nv.sum() * 4 + wl.Q * wl.k * 4)
+        # the visible scores read once (fp32 or bf16), the index lists written
+        sb = 2 if wl.scores == "bf16" else 4
+        w["topk_bytes"] = B * (nv.sum() * sb + wl.Q * wl.k * 4)
         sel = np.minimum(wl.k, nv)
         if wl.attend == "raw":  # the m raw tokens of every selected block
             keys = sel * m + win
@@ -430,6 +431,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
             with_clocks=True, want_cpu=False):
     """Time one workload: the whole step as a CUDA graph, each part in a graph
     of its own, and the end-to-end path with host copies."""
+    import numpy as np
     from long_context_sparse_25_b300 import csa, synth
     from long_context_sparse_25_b300.pipeline import Step
 
@@ -589,6 +591,23 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne, dist, dev)
     units = job_units(wl, world)
+    recall = None
+    if wl.scores == "bf16":
+        # how much of the fp32-score selection the bf16-score selection keeps
+        # (the same inputs, the step run once with each score dtype)
+        ref_step = Step(wl.replace(scores="f32"), inp)
+        with torch.cuda.stream(stream):
+            step.run(stream=stream)
+            ref_step.run(stream=stream)
+        torch.cuda.synchronize()
+        csa.device_status(stream)
+        a16, a32 = step.selected().cpu().numpy(), ref_step.selected().cpu().numpy()
+        hits = sum(np.intersect1d(a16[b, i], a32[b, i][a32[b, i] >= 0]).size
+                   for b in range(wl.B) for i in range(wl.Q))
+        total = int((a32 >= 0).sum())
+        recall = {"value": hits / total, "of": "the fp32-score top-k sets, same inputs",
+                  "sets": wl.B * wl.Q}
+        del ref_step
     cpu = None
     if want_cpu:
         torch.cuda.synchronize()
@@ -597,7 +616,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
            "cpu_baseline": cpu,
            "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
-           "launches_per_step": step.launches_per_step()}
+           "launches_per_step": step.launches_per_step(), "recall_vs_f32": recall}
     del step, step2, inp, inp2, g_full, g_full2, g_part, host_in, host_out
     gc.collect()
     torch.cuda.empty_cache()
@@ -904,7 +923,8 @@ def run_ours(args, wl):
                 "steps": steps, "per_part_ms": r["per_part_ms"],
                 "roofline": roofline(sw, r["per_part_ms"], r["ms"], peaks, peak_kind),
                 "e2e": r["e2e"], "gpu_launches": r["launches_per_step"] * steps,
-                "cpu_baseline": r["cpu_baseline"]}
+                "cpu_baseline": r["cpu_baseline"],
+                **({"recall_vs_f32": r["recall_vs_f32"]} if r.get("recall_vs_f32") else {})}
 
     prefill = None
     others = {}
@@ -913,7 +933,7 @@ def run_ours(args, wl):
         if not args.no_others:
             # the other rows of the path: HCA prefill and decode, mixed-precision decode
             for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k",
-                         "csa_decode_raw_1m"):
+                         "csa_decode_raw_1m", "csa_decode_1m_bf16s"):
                 others[name] = secondary(name, min(args.steps, 10))
             # a CSA layer and an HCA layer decoding token by token
             others["hybrid_decode_1m"] = measure_hybrid(args, synth.HYBRID["hybrid_decode_1m"],
@@ -971,8 +991,10 @@ def main():
     if args.workload in synth.GPROJ and args.impl == "ours":
         torch.cuda.set_device(0)
         peaks, peak_kind = _peaks()
-        row = measure_gproj(args, synth.GPROJ[args.workload], torch.device("cuda", 0), peaks,
-                            peak_kind, steps=args.steps)
+        gw = synth.GPROJ[args.workload]
+        if args.context:
+            gw = gw.replace(T=args.context)
+        row = measure_gproj(args, gw, torch.device("cuda", 0), peaks, peak_kind, steps=args.steps)
         print(json.dumps(row), flush=True)
         return
     if args.workload in synth.HYBRID and args.impl == "ours":

@@ -150,6 +150,18 @@ int csa_index(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const f
               float* scores, csa_stream_t stream);
 
 /*
+ * csa_index_ex -- csa_index with the scores stored in `scores_dtype`:
+ * CSA_F32 (as csa_index) or CSA_BF16 ([csdn] section "V4 的其他升级": the
+ * index scores drop to BF16, which doubles the speed of the top-k).  BF16
+ * scores are the fp32 scores rounded to the nearest bf16 (ties to even);
+ * invisible entries hold -inf.  `scores` is [B, Q, N] of that dtype.
+ * Errors: as csa_index; CSA_ERR_UNSUPPORTED for another scores_dtype.
+ */
+int csa_index_ex(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const float* q_scale,
+                 const float* w, const csa_rows* keys, int64_t q_pos0, int Q, int64_t N,
+                 void* scores, csa_dtype scores_dtype, csa_stream_t stream);
+
+/*
  * csa_topk -- keep the best entries per query ([csdn] section "V4 改进一：CSA
  * 与 HCA", second CSA step; [yudong] 2.2 Step 3):
  *   idx[b,i,:] = the min(k, n_vis) indices s < n_vis = min(N, n_vis(q_pos0+i))
@@ -163,6 +175,15 @@ int csa_index(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const f
  */
 int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, int64_t N,
              int32_t* idx, void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_topk_ex -- csa_topk over scores of dtype `scores_dtype` (CSA_F32 or
+ * CSA_BF16, as written by csa_index_ex).  BF16 scores tie far more often;
+ * ties still go to the lower index.  Same workspace as csa_topk.
+ * Errors: as csa_topk; CSA_ERR_UNSUPPORTED for another scores_dtype.
+ */
+int csa_topk_ex(const csa_params* p, const void* scores, csa_dtype scores_dtype, int64_t q_pos0,
+                int Q, int64_t N, int32_t* idx, void* ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
  * csa_topk_noalloc -- csa_topk for callers that cannot allocate device memory
@@ -286,6 +307,9 @@ typedef struct {
    * entries (csa_attend). */
   const void* raw_all;
   int64_t raw_all_rows;
+  /* Dtype of the indexer scores in the workspace: CSA_F32 (0, the default of
+   * a zero-initialised struct) or CSA_BF16 (csa_index_ex). */
+  csa_dtype score_dtype;
 } csa_forward_args;
 
 /*

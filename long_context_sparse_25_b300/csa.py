@@ -61,7 +61,7 @@ class ForwardArgs(C.Structure):
                 ("q_idx_dtype", C.c_int), ("q_idx_scale", C.c_void_p), ("w", C.c_void_p),
                 ("q_pos0", C.c_int64), ("Q", C.c_int), ("kv", Rows), ("keys", Rows),
                 ("n_cached", C.c_int64), ("out", C.c_void_p), ("out_dtype", C.c_int),
-                ("raw_all", C.c_void_p), ("raw_all_rows", C.c_int64)]
+                ("raw_all", C.c_void_p), ("raw_all_rows", C.c_int64), ("score_dtype", C.c_int)]
 
 
 _P, _I, _I64, _SZ = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
@@ -78,6 +78,9 @@ _SIGS = {
     "csa_forward": [C.POINTER(Params), C.POINTER(ForwardArgs), _P, _SZ, _P],
     "csa_topk_noalloc": [C.POINTER(Params), _P, _I64, _I, _I64, _P, _P],
     "csa_group_proj": [_P, _I64, _I, _I, _P, _I, _I, _P, _I, _P],
+    "csa_index_ex": [C.POINTER(Params), _P, _I, _P, _P, C.POINTER(Rows), _I64, _I, _I64, _P, _I,
+                     _P],
+    "csa_topk_ex": [C.POINTER(Params), _P, _I, _I64, _I, _I64, _P, _P, _SZ, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -163,7 +166,13 @@ def compress(x, gate, bias, m, s_begin, s_end, out: Rows, x_pos0=0, stream=None)
 
 
 def index(p: Params, q_idx, w, keys: Rows, q_pos0, N, scores, q_scale=None, stream=None):
+    """csa_index (fp32 scores) or csa_index_ex (bf16 scores), by scores' dtype."""
     Q = q_idx.shape[1]
+    if scores.dtype == torch.bfloat16:
+        _check(lib.csa_index_ex(C.byref(p), _ptr(q_idx), dtype_code(q_idx), _ptr(q_scale),
+                                _ptr(w), C.byref(keys), q_pos0, Q, N, _ptr(scores), BF16,
+                                _stream(stream)))
+        return
     _check(lib.csa_index(C.byref(p), _ptr(q_idx), dtype_code(q_idx), _ptr(q_scale), _ptr(w),
                          C.byref(keys), q_pos0, Q, N, _ptr(scores), _stream(stream)))
 
@@ -173,8 +182,8 @@ def topk(p: Params, scores, q_pos0, idx, ws=None, stream=None):
     nbytes = workspace_size(p, WS_TOPK, Q, N)
     if ws is None:
         ws = _workspace(nbytes, scores.device)
-    _check(lib.csa_topk(C.byref(p), _ptr(scores), q_pos0, Q, N, _ptr(idx), _ptr(ws),
-                        0 if ws is None else ws.numel(), _stream(stream)))
+    _check(lib.csa_topk_ex(C.byref(p), _ptr(scores), dtype_code(scores), q_pos0, Q, N, _ptr(idx),
+                           _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 TOPK_NOALLOC_MAX_BYTES = 16 << 20  # CSA_TOPK_NOALLOC_MAX_BYTES of include/csa.h
@@ -220,14 +229,16 @@ def hca(p: Params, q, kv: Rows, raw: Rows | None, raw_pos0, q_pos0, N, out, ws=N
 
 
 def forward_args(*, x, gate, bias, xi, gate_i, bias_i, raw_pos0, q, q_idx, w, q_pos0, kv: Rows,
-                 keys: Rows, n_cached, out, q_idx_scale=None, raw_all=None) -> ForwardArgs:
+                 keys: Rows, n_cached, out, q_idx_scale=None, raw_all=None,
+                 score_dtype=F32) -> ForwardArgs:
     """Arguments of csa_forward.  raw_all (raw rows of every position from 0)
-    selects the raw-token attention."""
+    selects the raw-token attention; score_dtype BF16 stores the indexer
+    scores in bf16."""
     return ForwardArgs(_ptr(x), _ptr(gate), _ptr(bias), _ptr(xi), _ptr(gate_i), _ptr(bias_i),
                        dtype_code(x), x.shape[1], raw_pos0, _ptr(q), dtype_code(q), _ptr(q_idx),
                        dtype_code(q_idx), _ptr(q_idx_scale), _ptr(w), q_pos0, q.shape[1], kv, keys,
                        n_cached, _ptr(out), dtype_code(out), _ptr(raw_all),
-                       0 if raw_all is None else raw_all.shape[1])
+                       0 if raw_all is None else raw_all.shape[1], score_dtype)
 
 
 def group_proj(o, w, y, stream=None):

@@ -196,6 +196,14 @@ int csa_compress(const void* x, const void* gate, csa_dtype in_dtype, const floa
 int csa_index(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const float* q_scale,
               const float* w, const csa_rows* keys, int64_t q_pos0, int Q, int64_t N,
               float* scores, csa_stream_t stream) {
+  return csa_index_ex(p, q_idx, q_dtype, q_scale, w, keys, q_pos0, Q, N, scores, CSA_F32, stream);
+}
+
+int csa_index_ex(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const float* q_scale,
+                 const float* w, const csa_rows* keys, int64_t q_pos0, int Q, int64_t N,
+                 void* scores, csa_dtype scores_dtype, csa_stream_t stream) {
+  REQUIRE(scores_dtype == CSA_F32 || scores_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
+          "scores must be F32 or BF16");
   CHECK(check_params(p, true, false));
   CHECK(check_positions(q_pos0, Q, N, p->m));
   CHECK(check_rows(keys, "keys", p->d_I, N, true, p->d_I));
@@ -209,12 +217,19 @@ int csa_index(const csa_params* p, const void* q_idx, csa_dtype q_dtype, const f
   CHECK_PTR(scores);
   if (q_dtype == CSA_E4M3) CHECK_PTR(q_scale);
   return cuda_status(launch_index(*p, q_idx, q_dtype, q_scale, w, *keys, q_pos0, Q, N, scores,
-                                  (cudaStream_t)stream),
+                                  scores_dtype == CSA_BF16, (cudaStream_t)stream),
                      "csa_index");
 }
 
 int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, int64_t N,
              int32_t* idx, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  return csa_topk_ex(p, scores, CSA_F32, q_pos0, Q, N, idx, ws, ws_bytes, stream);
+}
+
+int csa_topk_ex(const csa_params* p, const void* scores, csa_dtype scores_dtype, int64_t q_pos0,
+                int Q, int64_t N, int32_t* idx, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  REQUIRE(scores_dtype == CSA_F32 || scores_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
+          "scores must be F32 or BF16");
   CHECK(check_params(p, false, true));
   CHECK(check_positions(q_pos0, Q, N, p->m));
   if (Q == 0) return ok();
@@ -226,7 +241,8 @@ int csa_topk(const csa_params* p, const float* scores, int64_t q_pos0, int Q, in
     REQUIRE(ws && ws_bytes >= need, CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
     REQUIRE(aligned16(ws), CSA_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   }
-  return cuda_status(launch_topk(*p, scores, q_pos0, Q, N, idx, ws, (cudaStream_t)stream),
+  return cuda_status(launch_topk(*p, scores, scores_dtype == CSA_BF16, q_pos0, Q, N, idx, ws,
+                                 (cudaStream_t)stream),
                      "csa_topk");
 }
 
@@ -285,7 +301,7 @@ extern "C" int csa_topk_noalloc(const csa_params* p, const float* scores, int64_
           need, (size_t)CSA_TOPK_NOALLOC_MAX_BYTES);
   void* ws = nullptr;
   if (need) CHECK(noalloc_scratch(&ws));
-  return cuda_status(launch_topk(*p, scores, q_pos0, Q, N, idx, ws, (cudaStream_t)stream),
+  return cuda_status(launch_topk(*p, scores, false, q_pos0, Q, N, idx, ws, (cudaStream_t)stream),
                      "csa_topk_noalloc");
 }
 
@@ -446,10 +462,13 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
   REQUIRE((a->q_idx_dtype == CSA_E4M3) == (a->keys.dtype == CSA_E4M3), CSA_ERR_UNSUPPORTED,
           "q_idx and keys must both be e4m3 or both not");
   if (a->q_idx_dtype == CSA_E4M3) CHECK_PTR(a->q_idx_scale);
+  REQUIRE(a->score_dtype == CSA_F32 || a->score_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
+          "score_dtype must be F32 or BF16");
+  const bool bf16_scores = a->score_dtype == CSA_BF16;
 
   cudaStream_t st = (cudaStream_t)stream;
   char* w8 = reinterpret_cast<char*>(ws);
-  float* scores = reinterpret_cast<float*>(w8);
+  void* scores = w8;  // fp32 or bf16; the region is sized for fp32
   w8 += align256((size_t)p->B * a->Q * N * sizeof(float));
   int32_t* idx = reinterpret_cast<int32_t*>(w8);
   w8 += align256((size_t)p->B * a->Q * (size_t)p->k * sizeof(int32_t));
@@ -463,9 +482,9 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
     if (e != cudaSuccess) return cuda_status(e, "csa_forward/compress");
   }
   e = launch_index(*p, a->q_idx, a->q_idx_dtype, a->q_idx_scale, a->w, a->keys, a->q_pos0, a->Q, N,
-                   scores, st, /*fill_invisible=*/false);
+                   scores, bf16_scores, st, /*fill_invisible=*/false);
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/index");
-  e = launch_topk(*p, scores, a->q_pos0, a->Q, N, idx, rest, st);
+  e = launch_topk(*p, scores, bf16_scores, a->q_pos0, a->Q, N, idx, rest, st);
   if (e != cudaSuccess) return cuda_status(e, "csa_forward/topk");
   if (mode == kAttendRawBlocks)
     e = launch_attend(*p, a->q, a->q_dtype, raw_all, raw_all, 0, idx, mode, a->q_pos0, a->Q, N,

@@ -302,12 +302,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// `count` arrivals on `bar` at once (for the producers that do not take part
-// in a TMA chunk).
-__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(count)
-               : "memory");
-}
 
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -432,17 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!okw) return false;
         const uint32_t dst = tc::smem_u32(sRing + pslot * kChunk);
         if (!kE4M3 && t.tma) {
-          // one TMA box: thread 0 makes every producer's arrival (its own with
-          // the byte count) as it issues the copy, so the chunk's barrier
-          // completes on the bytes alone -- also when another producer gives
-          // up -- and the box can be waited for on the way out
+          // one TMA box: the chunk's barrier completes on its bytes and on
+          // every producer's own arrival (thread 0's carries the byte count).
+          // Each producer arrives itself, after its warp saw the slot
+          // released: a warp that skipped the chunks of a run of boxes could
+          // fall two fills behind the ring, where a parity wait takes the
+          // release it waits for to be still pending.
           if (pt == 0) {
             tc::mbar_expect_tx(&ring_full[pslot], kChunk);
-            mbar_arrive_n(&ring_full[pslot], kProd - 1);
             tma_mask |= 1u << pslot;
             tma_par = (tma_par & ~(1u << pslot)) | (pph << pslot);
             tc::tma_load_2d(sRing + pslot * kChunk, t.tma == 1 ? &tm_kv : &tm_raw,
                             &ring_full[pslot], c * 64, t.tma_y);
+          } else {
+            tc::mbar_arrive(&ring_full[pslot]);
           }
         } else if (kE4M3) {
           // every load of the chunk in flight first, then the conversions
@@ -617,7 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every copy must land before the CTA can exit: this thread's cp.async
       // (their arrivals on the ring barriers happen by themselves), and (pt 0)
       // the Q load and the ring's TMA boxes not yet known to have landed
-      // (only after an error: otherwise the MMA issuer waited for all of them)
+      // (only after an error: otherwise the MMA issuer waited for all of them;
+      // a box whose barrier also misses the arrival of a producer that gave up
+      // is waited for up to the bounded-wait limit, long after it landed)
       cp_async_wait<0>();
       if (pt == 0) {
         for (int c = 0; c < a.nc; ++c) tc::mbar_drain(&q_full[c], 0);

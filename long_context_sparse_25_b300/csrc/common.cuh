@@ -91,10 +91,12 @@ cudaError_t launch_compress_pair(const void* x0, const void* g0, const float* bi
 
 // fill_invisible: write -inf for entries beyond each query's visibility (the
 // fused forward skips it: top-k never reads them).
+// scores_bf16: the scores are stored as bf16 (round to nearest even; -inf
+// stays -inf) instead of fp32.
 cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                          const float* q_scale, const float* w, const csa_rows& keys,
-                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
-                         bool fill_invisible = true);
+                         int64_t q_pos0, int Q, int64_t N, void* scores, bool scores_bf16,
+                         cudaStream_t st, bool fill_invisible = true);
 
 // Test aid (csa_debug_stall_next): true once, for the first launch of the
 // named kernel after the aid was armed, which then clears it.
@@ -113,8 +115,9 @@ cudaError_t launch_group_proj(const void* o, int64_t T, int H, int D_v, const vo
 
 size_t topk_workspace(const csa_params& p, int Q, int64_t N);
 int topk_launches(const csa_params& p, int Q, int64_t N);
-cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0, int Q, int64_t N,
-                        int32_t* idx, void* ws, cudaStream_t st);
+// bf16: the scores are bf16 bit patterns (16-bit keys) instead of fp32.
+cudaError_t launch_topk(const csa_params& p, const void* scores, bool bf16, int64_t q_pos0, int Q,
+                        int64_t N, int32_t* idx, void* ws, cudaStream_t st);
 
 // Key list of the attention: the selected entries (CSA), every visible
 // entry (HCA), or the m raw tokens of every selected entry's block (the

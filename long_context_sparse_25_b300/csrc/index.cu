@@ -18,8 +18,8 @@ namespace csa {
 bool index_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& keys, int Q);
 cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                             const float* q_scale, const float* w, const csa_rows& keys,
-                            int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
-                            bool fill_invisible);
+                            int64_t q_pos0, int Q, int64_t N, void* scores, bool scores_bf16,
+                            cudaStream_t st, bool fill_invisible);
 
 namespace {
 
@@ -28,7 +28,7 @@ constexpr int kKeysPerCta = 128;
 __global__ void __launch_bounds__(kKeysPerCta) index_simt_kernel(
     const void* __restrict__ q_idx, csa_dtype q_dtype, const float* __restrict__ q_scale,
     const float* __restrict__ w, RowView keys, int H_I, int d_I, int m, int64_t q_pos0, int Q,
-    int64_t N, float* __restrict__ scores) {
+    int64_t N, void* __restrict__ scores, int scores_bf16) {
   extern __shared__ float sm[];
   float* qs = sm;                      // [H_I][d_I]
   float* ws = sm + (size_t)H_I * d_I;  // [H_I]
@@ -64,19 +64,22 @@ __global__ void __launch_bounds__(kKeysPerCta) index_simt_kernel(
     }
     out = acc;
   }
-  scores[qrow * N + s] = out;
+  if (scores_bf16)
+    reinterpret_cast<uint16_t*>(scores)[qrow * N + s] = __bfloat16_as_ushort(__float2bfloat16_rn(out));
+  else
+    reinterpret_cast<float*>(scores)[qrow * N + s] = out;
 }
 
 }  // namespace
 
 cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                          const float* q_scale, const float* w, const csa_rows& keys,
-                         int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
-                         bool fill_invisible) {
+                         int64_t q_pos0, int Q, int64_t N, void* scores, bool scores_bf16,
+                         cudaStream_t st, bool fill_invisible) {
   if (N <= 0 || Q <= 0 || p.B <= 0) return cudaSuccess;
   if (index_tc_supported(p, q_dtype, keys, Q))
-    return launch_index_tc(p, q_idx, q_dtype, q_scale, w, keys, q_pos0, Q, N, scores, st,
-                           fill_invisible);
+    return launch_index_tc(p, q_idx, q_dtype, q_scale, w, keys, q_pos0, Q, N, scores, scores_bf16,
+                           st, fill_invisible);
   const int64_t blocks = ceil_div(N, kKeysPerCta) * Q * p.B;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)blocks);
@@ -87,7 +90,8 @@ cudaError_t launch_index(const csa_params& p, const void* q_idx, csa_dtype q_dty
     if (e != cudaSuccess) return e;
   }
   index_simt_kernel<<<grid, kKeysPerCta, smem, st>>>(q_idx, q_dtype, q_scale, w, make_view(keys),
-                                                     p.H_I, p.d_I, p.m, q_pos0, Q, N, scores);
+                                                     p.H_I, p.d_I, p.m, q_pos0, Q, N, scores,
+                                                     scores_bf16 ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,8 @@ struct TcArgs {
   const float* w;
   const float* q_scale;  // e4m3 only
   const float* k_scale;  // e4m3 only
-  float* scores;
+  void* scores;      // [B, Q, N] fp32, or bf16 bit patterns (scores_bf16)
+  int scores_bf16;
 };
 
 __device__ __forceinline__ int tiles_visible(const TcArgs& a, int qb) {
@@ -384,7 +385,12 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
         for (int ql = 0; ql < QPW; ++ql) {
           const int i = qb * a.NQ + qoff + ql;
           if (i >= a.Q) break;
-          a.scores[((int64_t)b * a.Q + i) * a.N + s] = s < nv_q[ql] ? sc[ql] * ks : -INFINITY;
+          const float v = s < nv_q[ql] ? sc[ql] * ks : -INFINITY;
+          const int64_t o = ((int64_t)b * a.Q + i) * a.N + s;
+          if (a.scores_bf16)
+            reinterpret_cast<uint16_t*>(a.scores)[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          else
+            reinterpret_cast<float*>(a.scores)[o] = v;
         }
       }
       ++acc_it;
@@ -399,12 +405,15 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
 
 // -inf for entries beyond each query's visibility (the causal part of a
 // prefill score matrix that the tensor-core kernel never touches).
-__global__ void fill_invisible_kernel(float* __restrict__ scores, int Q, int64_t N, int m,
+__global__ void fill_invisible_kernel(void* __restrict__ scores, int bf16, int Q, int64_t N, int m,
                                       int64_t q_pos0) {
   const int64_t row = blockIdx.x;  // b * Q + i
   const int i = (int)(row % Q);
   const int64_t nv = n_vis(q_pos0 + i, m);
-  for (int64_t s = nv + threadIdx.x; s < N; s += blockDim.x) scores[row * N + s] = -INFINITY;
+  for (int64_t s = nv + threadIdx.x; s < N; s += blockDim.x) {
+    if (bf16) reinterpret_cast<uint16_t*>(scores)[row * N + s] = 0xFF80u;  // bf16 -inf
+    else reinterpret_cast<float*>(scores)[row * N + s] = -INFINITY;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -475,8 +484,8 @@ cudaError_t index_tc_status(int* code, cudaStream_t st) {
 
 cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_dtype,
                             const float* q_scale, const float* w, const csa_rows& keys,
-                            int64_t q_pos0, int Q, int64_t N, float* scores, cudaStream_t st,
-                            bool fill_invisible) {
+                            int64_t q_pos0, int Q, int64_t N, void* scores, bool scores_bf16,
+                            cudaStream_t st, bool fill_invisible) {
   const bool fp8 = keys.dtype == CSA_E4M3;
   (void)q_dtype;
   TcArgs a{};
@@ -542,6 +551,7 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   a.q_scale = q_scale;
   a.k_scale = keys.scale;
   a.scores = scores;
+  a.scores_bf16 = scores_bf16 ? 1 : 0;
   a.stall = take_debug_stall(kStallIndex) ? 1 : 0;
 
   CUtensorMap tm_keys, tm_q;
@@ -576,7 +586,8 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (fill_invisible && !all_visible) {
-    fill_invisible_kernel<<<(unsigned)((int64_t)p.B * Q), 256, 0, st>>>(scores, Q, N, p.m, q_pos0);
+    fill_invisible_kernel<<<(unsigned)((int64_t)p.B * Q), 256, 0, st>>>(scores, scores_bf16 ? 1 : 0,
+                                                                        Q, N, p.m, q_pos0);
     e = cudaGetLastError();
   }
   return e;

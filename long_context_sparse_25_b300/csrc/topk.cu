@@ -14,10 +14,34 @@
 // Rows up to kSmemRow entries are staged once in shared memory; longer rows
 // (decode over 10^5..10^6 entries) are re-read from global memory / L2 in
 // each pass by one CTA, or split over several CTAs by the multi-CTA path.
+//
+// Scores stored in bf16 ("一文搞懂 DeepSeek" section "V4 的其他升级": bf16
+// index scores make the top-k selection twice as fast) take 16-bit keys,
+// the upper half of the fp32 key of the same value: two digit passes, and
+// half the bytes read per pass.
 #include "common.cuh"
 
 namespace csa {
 namespace {
+
+// Order-preserving key of score i of a row: fp32 scores give 32-bit keys,
+// bf16 scores (bit patterns) 16-bit keys.
+template <typename ST>
+struct ScoreKey;
+template <>
+struct ScoreKey<float> {
+  static constexpr int kBits = 32;
+  __device__ static __forceinline__ uint32_t at(const float* p, int64_t i) {
+    return score_key(__ldg(p + i));
+  }
+};
+template <>
+struct ScoreKey<uint16_t> {
+  static constexpr int kBits = 16;
+  __device__ static __forceinline__ uint32_t at(const uint16_t* p, int64_t i) {
+    return score_key(__uint_as_float((uint32_t)__ldg(p + i) << 16)) >> 16;
+  }
+};
 
 constexpr int kThreads = 1024;
 constexpr int kSmemRow = 16384;
@@ -52,8 +76,8 @@ struct BlockScan {
   }
 };
 
-template <bool kSmem>
-__global__ void __launch_bounds__(kThreads) topk_row_kernel(const float* __restrict__ scores,
+template <bool kSmem, typename ST>
+__global__ void __launch_bounds__(kThreads) topk_row_kernel(const ST* __restrict__ scores,
                                                             int64_t q_pos0, int Q, int64_t N,
                                                             int m, int k,
                                                             int32_t* __restrict__ idx) {
@@ -68,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float* __restr
   const int64_t nvv = n_vis(q_pos0 + i, m);
   const int64_t n = nvv < N ? nvv : N;
   const int kk = (int)(n < k ? n : k);
-  const float* srow = scores + row * N;
+  const ST* srow = scores + row * N;
   int32_t* orow = idx + row * (int64_t)k;
 
   for (int j = kk + threadIdx.x; j < k; j += blockDim.x) orow[j] = -1;
@@ -77,15 +101,15 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const float* __restr
     return;
   }
   if (kSmem) {
-    for (int64_t s = threadIdx.x; s < n; s += blockDim.x) row_keys[s] = score_key(srow[s]);
+    for (int64_t s = threadIdx.x; s < n; s += blockDim.x) row_keys[s] = ScoreKey<ST>::at(srow, s);
   }
   auto key_at = [&](int64_t s) -> uint32_t {
-    return kSmem ? row_keys[s] : score_key(__ldg(srow + s));
+    return kSmem ? row_keys[s] : ScoreKey<ST>::at(srow, s);
   };
 
   uint32_t prefix = 0, mask = 0;
   int need = kk;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = ScoreKey<ST>::kBits - 8; shift >= 0; shift -= 8) {
     for (int j = threadIdx.x; j < 256; j += blockDim.x) hist[j] = 0;
     __syncthreads();
     for (int64_t s = threadIdx.x; s < n; s += blockDim.x) {
@@ -241,7 +265,8 @@ __device__ U radix_select(Get get, int64_t n, int need, int* hist, U* sh_prefix,
   return prefix;
 }
 
-__global__ void __launch_bounds__(1024) topk_sample_kernel(const float* __restrict__ scores,
+template <typename ST>
+__global__ void __launch_bounds__(1024) topk_sample_kernel(const ST* __restrict__ scores,
                                                            int64_t q_pos0, int Q, int64_t N, int m,
                                                            int k, LongRows lr) {
   __shared__ uint32_t keys[kSample];
@@ -252,19 +277,20 @@ __global__ void __launch_bounds__(1024) topk_sample_kernel(const float* __restri
   const int64_t n = row_visible(row, Q, q_pos0, m, N);
   if (n <= k) return;
   const int ns = n < kSample ? (int)n : kSample;
-  const float* srow = scores + row * N;
+  const ST* srow = scores + row * N;
   for (int j = threadIdx.x; j < ns; j += blockDim.x)
-    keys[j] = score_key(__ldg(srow + (int64_t)j * n / ns));
+    keys[j] = ScoreKey<ST>::at(srow, (int64_t)j * n / ns);
   __syncthreads();
   int64_t r = (4 * (int64_t)k * ns + n - 1) / n;
   if (r > ns) r = ns;
   if (r < 1) r = 1;
-  const uint32_t tau = radix_select<uint32_t, 32>([&](int64_t i) { return keys[i]; }, ns, (int)r,
-                                                  hist, &sh_prefix, &sh_need);
+  const uint32_t tau = radix_select<uint32_t, ScoreKey<ST>::kBits>(
+      [&](int64_t i) { return keys[i]; }, ns, (int)r, hist, &sh_prefix, &sh_need);
   if (threadIdx.x == 0) lr.tau[row] = tau;
 }
 
-__global__ void __launch_bounds__(512, 4) topk_filter_kernel(const float* __restrict__ scores,
+template <typename ST>
+__global__ void __launch_bounds__(512, 4) topk_filter_kernel(const ST* __restrict__ scores,
                                                           int64_t q_pos0, int Q, int64_t N, int m,
                                                           int k, LongRows lr) {
   const int64_t row = blockIdx.y;
@@ -279,7 +305,7 @@ __global__ void __launch_bounds__(512, 4) topk_filter_kernel(const float* __rest
   w0 += s0;
   w1 += s0;
   // positions within the row fit 32 bits (rows are < 2^31 entries)
-  const float* wrow = scores + row * N + w0;
+  const ST* wrow = scores + row * N + w0;
   unsigned long long* cand = lr.cand + row * N + w0;
   const int len = (int)(w1 - w0), pos0 = (int)w0;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -289,7 +315,7 @@ __global__ void __launch_bounds__(512, 4) topk_filter_kernel(const float* __rest
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int t = base + j * 32 + lane;
-      key[j] = t < len ? score_key(__ldg(wrow + t)) : 0u;
+      key[j] = t < len ? ScoreKey<ST>::at(wrow, t) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -336,7 +362,8 @@ __device__ int list_offsets(const int* cnt, int L, int* off, int* warp_sums) {
   return total;
 }
 
-__global__ void __launch_bounds__(1024) topk_final_kernel(const float* __restrict__ scores,
+template <typename ST>
+__global__ void __launch_bounds__(1024) topk_final_kernel(const ST* __restrict__ scores,
                                                           int64_t q_pos0, int Q, int64_t N, int m,
                                                           int k, LongRows lr,
                                                           int32_t* __restrict__ idx) {
@@ -364,18 +391,18 @@ __global__ void __launch_bounds__(1024) topk_final_kernel(const float* __restric
   }
   __syncthreads();
   const int nc = sh_nc;
-  const float* srow = scores + row * N;
+  const ST* srow = scores + row * N;
   if (nc < kk) {
     // fewer than kk keys reached tau: exact select over the whole row (the
     // kk-th largest key, then every larger key and the lowest-index equal
     // ones, in index order)
-    const uint32_t T = radix_select<uint32_t, 32>(
-        [&](int64_t i) { return score_key(__ldg(srow + i)); }, n, kk, hist, &sh_prefix32, &sh_need);
+    const uint32_t T = radix_select<uint32_t, ScoreKey<ST>::kBits>(
+        [&](int64_t i) { return ScoreKey<ST>::at(srow, i); }, n, kk, hist, &sh_prefix32, &sh_need);
     const int need_eq = sh_need;  // keys equal to T still needed
     int taken = 0, eq_seen = 0;
     for (int64_t base = 0; base < n; base += blockDim.x) {
       const int64_t t = base + threadIdx.x;
-      const uint32_t kx = t < n ? score_key(__ldg(srow + t)) : 0u;
+      const uint32_t kx = t < n ? ScoreKey<ST>::at(srow, t) : 0u;
       const int gt = (t < n && kx > T) ? 1 : 0;
       const int eq = (t < n && kx == T) ? 1 : 0;
       int eq_tot, take_tot;
@@ -405,7 +432,7 @@ __global__ void __launch_bounds__(1024) topk_final_kernel(const float* __restric
   __syncthreads();
   // the key of the kk-th largest candidate, and how many keys equal to it
   // are needed: the lowest-index ones (candidates are in index order)
-  const uint32_t T = radix_select<uint32_t, 32>(
+  const uint32_t T = radix_select<uint32_t, ScoreKey<ST>::kBits>(
       [&](int64_t i) { return (uint32_t)((in_smem ? cbuf[i] : cand_at(i)) >> 32); }, nc, kk, hist,
       &sh_prefix32, &sh_need);
   const int need_eq = sh_need;
@@ -467,8 +494,11 @@ size_t topk_workspace(const csa_params& p, int Q, int64_t N) {
 
 int topk_launches(const csa_params& p, int Q, int64_t N) { return use_long_rows(p, Q, N) ? 3 : 1; }
 
-cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0, int Q,
-                        int64_t N, int32_t* idx, void* ws, cudaStream_t st) {
+namespace {
+
+template <typename ST>
+cudaError_t launch_topk_t(const csa_params& p, const ST* scores, int64_t q_pos0, int Q, int64_t N,
+                          int32_t* idx, void* ws, cudaStream_t st) {
   const int64_t rows = (int64_t)p.B * Q;
   if (rows <= 0) return cudaSuccess;
   if (use_long_rows(p, Q, N)) {
@@ -480,30 +510,40 @@ cudaError_t launch_topk(const csa_params& p, const float* scores, int64_t q_pos0
     lr.tau = reinterpret_cast<uint32_t*>(w + off[0]);
     lr.cnt = reinterpret_cast<int*>(w + off[1]);
     lr.cand = reinterpret_cast<unsigned long long*>(w + off[2]);
-    topk_sample_kernel<<<(unsigned)rows, 1024, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
+    topk_sample_kernel<ST><<<(unsigned)rows, 1024, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
     dim3 g((unsigned)lr.S, (unsigned)rows);
-    topk_filter_kernel<<<g, 32 * kWarpsB, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
+    topk_filter_kernel<ST><<<g, 32 * kWarpsB, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr);
     const size_t smem = kCandSmem * sizeof(unsigned long long) + kMaxLists * sizeof(int);
-    cudaError_t e = cudaFuncSetAttribute(topk_final_kernel,
+    cudaError_t e = cudaFuncSetAttribute(topk_final_kernel<ST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_final_kernel<<<(unsigned)rows, 1024, smem, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr, idx);
+    topk_final_kernel<ST><<<(unsigned)rows, 1024, smem, st>>>(scores, q_pos0, Q, N, p.m, p.k, lr,
+                                                             idx);
     return cudaGetLastError();
   }
   if (N <= kSmemRow) {
     size_t smem = (size_t)N * sizeof(uint32_t);
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(topk_row_kernel<true>,
+      cudaError_t e = cudaFuncSetAttribute(topk_row_kernel<true, ST>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    topk_row_kernel<true><<<(unsigned)rows, kThreads, smem, st>>>(scores, q_pos0, Q, N, p.m, p.k,
-                                                                  idx);
+    topk_row_kernel<true, ST><<<(unsigned)rows, kThreads, smem, st>>>(scores, q_pos0, Q, N, p.m,
+                                                                     p.k, idx);
   } else {
-    topk_row_kernel<false><<<(unsigned)rows, kThreads, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k,
-                                                                idx);
+    topk_row_kernel<false, ST><<<(unsigned)rows, kThreads, 0, st>>>(scores, q_pos0, Q, N, p.m, p.k,
+                                                                   idx);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const csa_params& p, const void* scores, bool bf16, int64_t q_pos0, int Q,
+                        int64_t N, int32_t* idx, void* ws, cudaStream_t st) {
+  if (bf16)
+    return launch_topk_t(p, reinterpret_cast<const uint16_t*>(scores), q_pos0, Q, N, idx, ws, st);
+  return launch_topk_t(p, reinterpret_cast<const float*>(scores), q_pos0, Q, N, idx, ws, st);
 }
 
 }  // namespace csa

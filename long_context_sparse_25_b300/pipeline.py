@@ -58,7 +58,8 @@ class Step:
                 bias_i=inp["bias_i"], raw_pos0=wl.raw_pos0, q=inp["q"], q_idx=inp["q_idx"],
                 w=inp["w"], q_pos0=wl.q_pos0, kv=self.kv, keys=self.keys,
                 n_cached=self.n_cached, out=self.out, q_idx_scale=inp.get("q_idx_scale"),
-                raw_all=inp.get("x_all") if wl.attend == "raw" else None)
+                raw_all=inp.get("x_all") if wl.attend == "raw" else None,
+                score_dtype=csa.BF16 if wl.scores == "bf16" else csa.F32)
             nbytes = csa.workspace_size(self.p, csa.WS_FORWARD, wl.Q, N)
         else:
             nbytes = csa.workspace_size(self.p, csa.WS_HCA, wl.Q, N)
@@ -66,8 +67,12 @@ class Step:
 
     # views into the forward workspace (CSA only)
     def scores(self) -> torch.Tensor:
+        """The indexer scores in the forward workspace (fp32, or bf16 for a
+        bf16-score workload; the region is sized for fp32 either way)."""
         wl = self.wl
         n = wl.B * wl.Q * wl.N
+        if wl.scores == "bf16":
+            return self.ws[: n * 2].view(torch.bfloat16).view(wl.B, wl.Q, wl.N)
         return self.ws[: n * 4].view(torch.float32).view(wl.B, wl.Q, wl.N)
 
     def selected(self) -> torch.Tensor:

@@ -25,6 +25,8 @@ Workloads (sizes from the pages' configurations):
   raw-token attention: the raw KV rows of all 2^20 positions are resident
   (``x_all``), and each query attends over the 4 raw tokens of each of its
   1024 selected blocks plus the window.
+* ``csa_decode_1m_bf16s`` -- ``csa_decode_1m`` (same inputs) with the indexer
+  scores stored in bf16 and the top-k over those.
 * ``gproj_prefill_64k`` / ``gproj_decode_b32`` (``GPROJ``) -- the grouped
   output projection of the attention output of a 65,536-token prefill and of
   a 32-sequence decode step: 128 heads x 512 in 8 groups of 16 heads, each
@@ -70,6 +72,7 @@ class Workload:
     q_std: float = 1.0      # extra factor on Q (the tiny case folds 1/sqrt(128))
     softmax_scale: float | None = None
     attend: str = "entries"  # "entries" | "raw": the raw tokens of the selected blocks
+    scores: str = "f32"      # dtype of the indexer scores: "f32" | "bf16"
 
     @property
     def N(self) -> int:
@@ -121,6 +124,9 @@ WORKLOADS = {
     "csa_decode_raw_1m": Workload("csa_decode_raw_1m", "csa_decode", B=32, L=1 << 20, m=4, H=128,
                                   D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
                                   dtype="bf16", seed=2, attend="raw"),
+    "csa_decode_1m_bf16s": Workload("csa_decode_1m_bf16s", "csa_decode", B=32, L=1 << 20, m=4,
+                                    H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
+                                    dtype="bf16", seed=2, scores="bf16"),
 }
 
 # tensor ids (the generator of tensor `name` is seeded with seed * 1000 + id)

@@ -128,6 +128,64 @@ def check_scores(gpu: np.ndarray, ref: np.ndarray, check_invisible: bool = False
     return worst
 
 
+def _bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |x| (normal range)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 8)
+
+
+def check_scores_bf16(gpu: np.ndarray, ref: np.ndarray):
+    """GPU bf16 scores against the float64 scores: the pattern of -inf is the
+    oracle's, and every visible score is the bf16 rounding of a value within
+    1e-5 of the row scale of the exact score (fp32 accumulation, then one
+    rounding): |gpu - ref| <= 1e-5 * row scale + half a bf16 spacing."""
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(gpu), ~fin), "visibility pattern differs"
+    if not fin.any():
+        return 0.0
+    row_scale = np.where(fin, np.abs(ref), 0).max(axis=1, keepdims=True) + 1e-30
+    r = np.where(fin, ref, 0.0)
+    g = np.where(fin, gpu, 0.0)
+    bound = 1e-5 * row_scale + _bf16_half_ulp(r) * (1 + 1e-6) + 1e-6 * row_scale * 2.0 ** -8
+    excess = np.abs(g - r) - bound
+    worst = float(excess[fin].max())
+    assert worst <= 0, f"a bf16 score is {worst:.3e} beyond its rounding bound"
+    return worst
+
+
+def check_selection_bf16(sel_gpu: np.ndarray, ref_scores: np.ndarray, nvis: np.ndarray, k: int):
+    """Swap rule for bf16 scores: the oracle rounds its scores to bf16 and
+    selects on those (ties to the lower index); the GPU set has the same
+    size, is ascending and visible, and every entry in the symmetric
+    difference has an exact score within 1e-5 of the row scale plus one bf16
+    spacing of tau16, the oracle's kk-th best bf16 score (only entries whose
+    rounding can land on either side of tau16 may swap)."""
+    import oracle as O
+    r16 = O.round_to_bf16(ref_scores)
+    swaps = 0
+    for r in range(sel_gpu.shape[0]):
+        nv = int(min(nvis[r], ref_scores.shape[1]))
+        kk = min(k, nv)
+        row = sel_gpu[r]
+        got = row[:kk]
+        assert np.all(row[kk:] == -1), f"row {r}: padding"
+        assert np.all(got >= 0) and np.all(got < nv), f"row {r}: index out of range"
+        assert np.all(np.diff(got) > 0), f"row {r}: not ascending / duplicates"
+        if kk == 0:
+            continue
+        ref = O.topk_row(r16[r], nv, k)
+        tau16 = np.sort(r16[r, :nv])[nv - kk]
+        scale = np.abs(ref_scores[r, :nv]).max() + 1e-30
+        diff = np.setxor1d(got, ref)
+        for s in diff:
+            gap = abs(ref_scores[r, s] - tau16)
+            allowed = 1e-5 * scale + 2 * _bf16_half_ulp(np.array(tau16))
+            assert gap <= allowed, (f"row {r}: entry {s} swapped, exact score {ref_scores[r, s]:.6g} "
+                                    f"vs tau16 {tau16:.6g}")
+        swaps += diff.size // 2
+    return swaps
+
+
 def check_selection(sel_gpu: np.ndarray, ref_scores: np.ndarray, nvis: np.ndarray, k: int):
     """Swap rule: the GPU set has the oracle's size, is ascending and visible,
     and every entry in the symmetric difference with the oracle's set has an

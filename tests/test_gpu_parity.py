@@ -11,7 +11,8 @@ import oracle as O
 from long_context_sparse_25_b300 import csa, synth
 from long_context_sparse_25_b300.pipeline import Step
 
-from harness import (SeqOracle, check_out, check_scores, check_selection, f64)
+from harness import (SeqOracle, check_out, check_scores, check_scores_bf16, check_selection,
+                     check_selection_bf16, f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +34,11 @@ CSA_CASES = {
     # raw-token attention (the 4 raw tokens of every selected block, then the
     # window): decode over 5000 entries, and an 8K prefill
     "decode_raw": (W["csa_decode_raw_1m"].replace(B=3, L=20000), None),
+    # indexer scores stored in bf16: decode (multi-CTA top-k over 16-bit keys)
+    # and a prefill (one CTA per row)
+    "decode_bf16_scores": (W["csa_decode_1m_bf16s"].replace(B=3, L=80000), None),
+    "prefill_bf16_scores_ragged": (W["csa_prefill_64k"].replace(L=2051, Q=2051, k=32,
+                                                                scores="bf16"), 160),
     "prefill_raw_8k": (W["csa_prefill_64k"].replace(L=8192, Q=8192, attend="raw"), 24),
     # raw-token attention through the CUDA-core path (fp32)
     "tiny_raw_f32": (W["csa_tiny_f32"].replace(L=1024, Q=1024, attend="raw"), None),
@@ -90,8 +96,15 @@ def test_csa_forward_matches_oracle(case, cuda_device):
             assert np.array_equal(got_kv, o.new_kv), "entries differ from the oracle"
         # step 2: scores; step 3: selection; step 4: attention on the GPU's set
         ref_scores = o.scores(qs)
-        check_scores(scores[b, qs], ref_scores)
-        check_selection(sel[b, qs], ref_scores, O.n_vis(o.positions(qs), wl.m), wl.k)
+        if wl.scores == "bf16":
+            nv = O.n_vis(o.positions(qs), wl.m)
+            # the fused forward leaves the invisible part unwritten
+            vis = np.arange(wl.N)[None, :] < nv[:, None]
+            check_scores_bf16(np.where(vis, scores[b, qs], -np.inf), ref_scores)
+            check_selection_bf16(sel[b, qs], ref_scores, nv, wl.k)
+        else:
+            check_scores(scores[b, qs], ref_scores)
+            check_selection(sel[b, qs], ref_scores, O.n_vis(o.positions(qs), wl.m), wl.k)
         ref_out = o.attend(qs, sel[b, qs])
         check_out(out[b, qs], ref_out, wl.dtype == "f32", unit_scale=wl.outliers == 0)
 
@@ -146,6 +159,31 @@ def test_topk_bit_exact_on_oracle_scores(cuda_device):
         for b in range(B):
             ref = O.topk(s32[b].astype(np.float64), pos, m, k)
             assert np.array_equal(got[b], ref)
+
+
+def test_topk_bit_exact_on_oracle_bf16_scores(cuda_device):
+    """csa_topk_ex fed the oracle's bf16 scores (csa.topk with a bf16 tensor)
+    returns exactly the oracle's index lists: many ties (bf16 keeps 8 bits),
+    signed zeros, -inf beyond visibility; rows in shared memory, long rows
+    over several CTAs, rows shorter than k."""
+    rng = np.random.default_rng(11)
+    for (B, Q, N, k, m, q_pos0) in [(2, 37, 700, 64, 4, 2700), (1, 5, 20000, 1024, 4, 79999),
+                                     (3, 9, 300, 1024, 4, 1000), (2, 3, 262144, 1024, 4, 1048575),
+                                     (2, 7, 1001, 256, 4, 3998)]:
+        s = rng.standard_normal((B, Q, N))
+        s = np.where(rng.uniform(size=s.shape) < 0.05, 0.0, s)
+        s = np.where(rng.uniform(size=s.shape) < 0.05, -0.0, s)
+        s16 = O.round_to_bf16(s)
+        pos = q_pos0 + np.arange(Q)
+        nv = O.n_vis(pos, m)
+        s16 = np.where(np.arange(N)[None, None] < nv[None, :, None], s16, -np.inf)
+        dev = torch.from_numpy(O.encode_bf16(s16).view(np.int16)).view(torch.bfloat16).to(cuda_device)
+        p = csa.params(B, m, k=k)
+        idx = torch.empty((B, Q, k), dtype=torch.int32, device=cuda_device)
+        csa.topk(p, dev, q_pos0, idx)
+        got = idx.cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(got[b], O.topk(s16[b], pos, m, k)), (B, Q, N, b)
 
 
 def test_topk_long_row_whose_sample_misleads(cuda_device):
