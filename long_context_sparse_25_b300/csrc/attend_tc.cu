@@ -34,17 +34,18 @@
 // as the ring allows; the MMA issuer, after its wait, issues the proxy fence
 // that makes the rows visible to the tensor cores.  A tile whose 128 slots
 // are all valid consecutive entries (HCA) or all window slots is one TMA box
-// per chunk instead.  Mixed-precision caches (e4m3 codes with a row scale,
-// RoPE dims in bf16) are converted by the producers themselves: for QK^T each
-// dequantised key is split exactly into a bf16 high part and a bf16 low part
-// (one load per nope chunk fills two ring slots, both multiplied by the same
-// Q chunk), so the scores
-// see the key to about 2^-17; for PV the chunk holds the codes themselves
-// (exact in bf16) and the row scale is folded into P, which is split the same
-// way (PV runs on the high and on the low part).  The MMA order is S(0),
-// S(1), PV(0), S(2), PV(1), ... so the softmax of tile u overlaps S(u+1).  A
-// key row doubles as its value row: the same 128-byte swizzled chunk is
-// K-major for QK^T and MN-major for PV.
+// per chunk instead.  Mixed-precision caches (e4m3 codes with a row scale
+// c_j, RoPE dims in bf16) run in f16: the codes are exact in f16, so a code
+// chunk is the codes themselves (one conversion instruction per two codes),
+// and the row scale moves out of the keys: the tile holds S'_j = q_nope .
+// code_j + q_rope . (rope_j / c_j), the RoPE dims over the row scale split
+// exactly into an f16 high and low part (two ring slots that meet the same Q
+// chunk), and the softmax takes S_j = c_j S'_j.  P . V runs on the codes with
+// c_j folded into P, rounded once to f16.  Q is converted to f16 in shared
+// memory once per CTA.  The MMA order is S(0), S(1), PV(0), S(2), PV(1), ...
+// so the softmax of tile u overlaps S(u+1).  A key row doubles as its value
+// row: the same 128-byte swizzled chunk is K-major for QK^T and MN-major for
+// PV.
 //
 // Softmax: one thread per head row, log2 domain, running maximum updated only
 // when a tile's maximum exceeds it by more than 2^8 (then O and the running
@@ -64,6 +65,8 @@
 // rescale / epilogue.  Every mbarrier wait is bounded; a timeout is recorded
 // in a device error word and the kernel returns.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstring>
 
@@ -91,7 +94,7 @@ constexpr int kThreads = 256;        // + warps 4-7: softmax / epilogue
 struct AttArgs {
   int B, Q, H, D_qk, D_v, k, W, m;
   int nc;   // D_qk / 64
-  int nsc;  // key chunk loads per tile for QK^T (nc, plus nope/64 low parts for e4m3)
+  int nsc;  // key chunk slots per tile for QK^T (nc; e4m3: the RoPE chunks take two each)
   int nvc;  // D_v / 128: value chunks per half
   int dense;    // every visible entry (HCA)
   int rawblk;   // the raw tokens of the selected blocks (raw-token variant)
@@ -202,88 +205,76 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return l | (h << 16);
 }
 
-// Mixed-precision cache: 16 bytes (8 dims, from dim c*64 + uc*8) of one key
-// row of a chunk, as bf16, written by a producer thread itself.
-//   kHi:  dequantised nope dims rounded to bf16 (RoPE dims and window rows:
-//         their bf16 values);
-//   kLo:  the rounding error of kHi, rounded to bf16 (window rows, RoPE: 0);
-//   kVal: the e4m3 codes as bf16 (exact; the row scale goes into P), window
-//         and RoPE dims as they are.
-enum ChunkMode { kHi = 0, kLo = 1, kVal = 2 };
-
-// The raw 16 bytes (bf16 rows) or 8 bytes (e4m3 codes) of a unit, and the
-// row scale the codes need; split from the conversion so that a producer
-// thread can have all its loads of a chunk in flight at once.
-struct RawUnit {
-  uint4 v;
-  float sc;
-  int kind;  // 0: bf16 values, 1: e4m3 codes in v.x / v.y, 2: zeros
+// Mixed-precision cache: the 16 bytes (8 dims, from dim c*64 + uc*8) of one
+// key row that a producer thread writes into a chunk, as f16.  The raw unit
+// is loaded first (all of a chunk's loads in flight), converted after.
+struct MixUnit {
+  uint4 v;    // kind 0: 8 bf16 values; kind 1: 8 e4m3 codes in v.x, v.y
+  float inv;  // RoPE dims of an entry: 1 / row scale; else 1
+  int kind;
 };
 
-__device__ __forceinline__ RawUnit manual_load(const AttArgs& a, int64_t row, bool win, int c, int uc,
-                                               int mode) {
-  RawUnit r;
-  r.sc = 1.f;
+__device__ __forceinline__ MixUnit mix_load(const AttArgs& a, int64_t row, bool win, int c,
+                                            int uc) {
+  MixUnit r;
+  r.inv = 1.f;
   const int d0 = c * 64 + uc * 8;
-  if (win || d0 >= a.nope) {
-    r.kind = mode == kLo ? 2 : 0;
-    if (r.kind == 2) {
-      r.v = make_uint4(0u, 0u, 0u, 0u);
-    } else if (win) {
-      r.v = __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
-    } else {
-      const int rw = a.D_qk - a.nope;
-      r.v = __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
-    }
-    return r;
+  if (win) {  // a raw (window) row: bf16 values
+    r.kind = 0;
+    r.v = __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
+  } else if (d0 >= a.nope) {  // RoPE dims of an entry
+    r.kind = 0;
+    const int rw = a.D_qk - a.nope;
+    r.v = __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
+    r.inv = 1.f / __ldg(a.kscale + row);
+  } else {  // codes of an entry
+    r.kind = 1;
+    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(a.codes + row * a.nope + d0));
+    r.v = make_uint4(cv.x, cv.y, 0u, 0u);
   }
-  r.kind = 1;
-  const uint2 cv = __ldg(reinterpret_cast<const uint2*>(a.codes + row * a.nope + d0));
-  r.v = make_uint4(cv.x, cv.y, 0u, 0u);
-  if (mode != kVal) r.sc = __ldg(a.kscale + row);
   return r;
 }
 
-__device__ __forceinline__ uint4 manual_convert(const RawUnit& r, int mode) {
-  if (r.kind != 1) return r.v;
-  const uint32_t w2[2] = {r.v.x, r.v.y};
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// A code chunk or a value chunk: the codes exactly; bf16 values (window rows)
+// rounded to f16.
+__device__ __forceinline__ uint4 mix_f16(const MixUnit& r) {
   uint32_t o[4];
+  if (r.kind == 1) {
+    const uint32_t w2[2] = {r.v.x, r.v.y};
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t word = w2[e / 2];
-    const int sh = (e & 1) * 16;
-    // code * scale in fp32 is within 2^-24 of the exact product; the high
-    // part is its bf16 rounding, the low part the (exact) rest
-    float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * r.sc;
-    float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * r.sc;
-    if (mode == kLo) {
-      f0 -= __bfloat162float(__float2bfloat16_rn(f0));
-      f1 -= __bfloat162float(__float2bfloat16_rn(f1));
+    for (int e = 0; e < 4; ++e) {
+      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w2[e >> 1] >> ((e & 1) * 16)) & 0xffffu), __NV_E4M3);
+      o[e] = (uint32_t)h.x | ((uint32_t)h.y << 16);
     }
-    o[e] = pack_bf16(f0, f1);
+  } else {
+    const uint32_t w4[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = f16x2_bits(bf16_lo(w4[e]), bf16_hi(w4[e]));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Both parts of a unit for QK^T from one load: the kHi conversion and the
-// kLo conversion of the same unit (kind 0 / 2 rows: the values, zeros).
-__device__ __forceinline__ void manual_convert_pair(const RawUnit& r, uint4& hi, uint4& lo) {
-  if (r.kind != 1) {
-    hi = r.v;
-    lo = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  const uint32_t w2[2] = {r.v.x, r.v.y};
+// A RoPE chunk: value * inv split into an f16 high part and an f16 low part
+// (the rest, rounded): together within about 2^-22 of value * inv.
+__device__ __forceinline__ void mix_f16_pair(const MixUnit& r, uint4& hi, uint4& lo) {
+  const uint32_t w4[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
   uint32_t h[4], l[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const uint32_t word = w2[e / 2];
-    const int sh = (e & 1) * 16;
-    const float f0 = e4m3_to_f32((uint8_t)(word >> sh)) * r.sc;
-    const float f1 = e4m3_to_f32((uint8_t)(word >> (sh + 8))) * r.sc;
-    h[e] = pack_bf16(f0, f1);
-    l[e] = pack_bf16(f0 - __bfloat162float(__float2bfloat16_rn(f0)),
-                     f1 - __bfloat162float(__float2bfloat16_rn(f1)));
+    const float x0 = bf16_lo(w4[e]) * r.inv, x1 = bf16_hi(w4[e]) * r.inv;
+    const __half2 hh = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(hh);
+    h[e] = *reinterpret_cast<const uint32_t*>(&hh);
+    l[e] = f16x2_bits(x0 - hf.x, x1 - hf.y);
   }
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
@@ -325,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // phases behind (a parity wait cannot tell phase j from phase j + 2)
   uint64_t* o_done = mask_empty + 2;  // [2]
   uint64_t* mma_done = o_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* q_conv = mma_done + 1;  // e4m3: Q converted to f16 by every producer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_conv + 1);
   uint32_t* smask = tmem_slot + 4;  // [2][4] ballot words of the tile's valid slots
   float* svscale = reinterpret_cast<float*>(smask + 8);  // e4m3: [2][128] row scales of the tile
 
@@ -361,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&o_done[0], 1);
     tc::mbar_init(&o_done[1], 1);
     tc::mbar_init(mma_done, 1);
+    tc::mbar_init(q_conv, kProd);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tm_q);
     if (!kE4M3) {
@@ -398,6 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rowb = (int64_t)a.D_qk * 2;
       uint32_t pslot = 0, pph = 0;  // ring slot and the parity of its release
       bool ok = true;
+      if (kE4M3) {
+        // Q to f16 in place (elementwise, so the swizzle does not matter),
+        // then one arrival per producer thread on q_conv
+        for (int c = 0; c < a.nc && ok; ++c) ok = tc::mbar_wait(&q_full[c], 0, err, 13);
+        if (ok) {
+          for (int u = pt; u < a.nc * (int)(kChunk / 16); u += kProd) {
+            uint4* q4 = reinterpret_cast<uint4*>(sQ) + u;
+            const uint4 v = *q4;
+            *q4 = make_uint4(f16x2_bits(bf16_lo(v.x), bf16_hi(v.x)),
+                             f16x2_bits(bf16_lo(v.y), bf16_hi(v.y)),
+                             f16x2_bits(bf16_lo(v.z), bf16_hi(v.z)),
+                             f16x2_bits(bf16_lo(v.w), bf16_hi(v.w)));
+          }
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(q_conv);
+        }
+      }
       uint32_t tma_mask = 0, tma_par = 0;  // pt 0: slots whose last fill was TMA, and its parity
       // swizzled destination of each of this thread's units within a chunk;
       // only the last unit can fall outside the chunk (threads pt >= 64)
@@ -419,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tma;    // bf16 caches: 1 = 128 consecutive entry rows, 2 = 128 consecutive
         int tma_y;  //   raw rows (from tma_y), loaded by one TMA box per chunk; 0 = gathered
       };
-      auto issue_chunk = [&](int c, int mode, const TileRows& t) -> bool {
+      auto issue_chunk = [&](int c, const TileRows& t) -> bool {
         int okw = 1;
         if (lane == 0) okw = tc::mbar_wait(&ring_empty[pslot], pph ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -443,19 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (kE4M3) {
           // every load of the chunk in flight first, then the conversions
-          RawUnit raw[kUnits];
+          MixUnit raw[kUnits];
 #pragma unroll
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
-              raw[i] = manual_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7, mode);
+              raw[i] = mix_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7);
           }
 #pragma unroll
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
               *reinterpret_cast<uint4*>(sRing + pslot * kChunk + swz(unit >> 3, unit & 7)) =
-                  manual_convert(raw[i], mode);
+                  mix_f16(raw[i]);
           }
           tc::fence_proxy_async_smem();
           tc::mbar_arrive(&ring_full[pslot]);
@@ -473,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      // Mixed caches: the high and the low part of nope chunk c go to two
-      // consecutive slots from one load and one dequantisation.
+      // Mixed caches: the high and the low part of RoPE chunk c (over the row
+      // scale) go to two consecutive slots from one load.
       auto issue_pair = [&](int c, const TileRows& t) -> bool {
         const uint32_t s0 = pslot, p0 = pph;
         const uint32_t s1 = pslot + 1 == kRing ? 0 : pslot + 1;
@@ -485,19 +495,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mbar_wait(&ring_empty[s1], p1 ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) return false;
-        RawUnit raw[kUnits];
+        MixUnit raw[kUnits];
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
           const int unit = pt + kProd * i;
           if (unit < (int)(kChunk / 16))
-            raw[i] = manual_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7, kHi);
+            raw[i] = mix_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7);
         }
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
           const int unit = pt + kProd * i;
           if (unit < (int)(kChunk / 16)) {
             uint4 hi, lo;
-            manual_convert_pair(raw[i], hi, lo);
+            mix_f16_pair(raw[i], hi, lo);
             *reinterpret_cast<uint4*>(sRing + s0 * kChunk + dso[i]) = hi;
             *reinterpret_cast<uint4*>(sRing + s1 * kChunk + dso[i]) = lo;
           }
@@ -599,15 +609,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
-          // QK^T chunks: mixed caches first the (high, low) pairs of the nope
-          // chunks, then the RoPE chunks; bf16 caches the nc chunks in order
-          const int nlo = kE4M3 ? a.nsc - a.nc : 0;
+          // QK^T chunks: the nc chunks in order; mixed caches' RoPE chunks as
+          // (high, low) pairs
+          const int ncode = kE4M3 ? a.nope / 64 : a.nc;
+          for (int c = 0; c < ncode && ok; ++c) ok = issue_chunk(c, cur);
           if (kE4M3)
-            for (int c = 0; c < nlo && ok; ++c) ok = issue_pair(c, cur);
-          for (int c = nlo; c < a.nc && ok; ++c) ok = issue_chunk(c, kHi, cur);
+            for (int c = ncode; c < a.nc && ok; ++c) ok = issue_pair(c, cur);
         }
         if (u >= 1)
-          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, kVal, prev);
+          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, prev);
         prev = cur;
         if (u + 1 < n) tile_rows(u + 1, wnext, cur);
       }
@@ -627,8 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      const uint32_t id_s = tc::idesc(128, kT, 1, 1);
-      const uint32_t id_pv = tc::idesc(128, 64, 1, 1, 0, 1);
+      // bf16 operands, or f16 for mixed caches (format 1 / 0 of kind::f16)
+      const uint32_t fmt = kE4M3 ? 0u : 1u;
+      const uint32_t id_s = tc::idesc(128, kT, fmt, fmt);
+      const uint32_t id_pv = tc::idesc(128, 64, fmt, fmt, 0, 1);
       bool ok = true;
       // test aid: the producers' first loads are in flight while this waits
       if (a.stall && blockIdx.x == 0) ok = tc::flag_wait(&g_attend_never_set, tc::kStallNs, err, 28);
@@ -665,8 +677,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 16 keys per K step: 16 rows of 128 bytes
             const uint64_t bd = vd + (uint64_t)(ks * (2048 >> 4));
             tc::mma_bf16_ts(o_tmem, p_tmem + 8 * ks, bd, id_pv, (u > 0 || ks > 0) ? 1u : 0u);
-            if (kE4M3)  // the low part of P
-              tc::mma_bf16_ts(o_tmem, p_tmem + 64 + 8 * ks, bd, id_pv, 1u);
           }
           tc::mma_commit(&ring_empty[slot]);
           next_slot();
@@ -678,11 +688,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = u & 1;
         const uint32_t s_tmem = tmem + sb * 128;
         for (int cc = 0; cc < a.nsc && ok; ++cc) {
-          // the Q chunk this key chunk meets (the producers' order: mixed
-          // caches' (high, low) pairs of the nope chunks, then the rest)
-          const int nlo = kE4M3 ? a.nsc - a.nc : 0;
-          const int c = cc < 2 * nlo ? cc >> 1 : cc - nlo;
-          if (!((q_seen >> c) & 1u)) {
+          // the Q chunk this key chunk meets (the producers' order: the code
+          // chunks, then mixed caches' (high, low) pairs of the RoPE chunks)
+          const int ncode = kE4M3 ? a.nope / 64 : a.nc;
+          const int c = cc < ncode ? cc : ncode + ((cc - ncode) >> 1);
+          if (kE4M3) {
+            if (!q_seen && !tc::mbar_wait(q_conv, 0, err, 21)) { ok = false; break; }
+            q_seen = 1;
+          } else if (!((q_seen >> c) & 1u)) {
             if (!tc::mbar_wait(&q_full[c], 0, err, 21)) { ok = false; break; }
             q_seen |= 1u << c;
           }
@@ -743,7 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kT; ++j) {
         const bool v = (bal[j >> 5] >> (j & 31)) & 1u;
-        x[j] = v ? x[j] * a.c_log2 : -INFINITY;
+        // mixed caches: the tile holds S' = S / c_j
+        x[j] = v ? x[j] * (kE4M3 ? a.c_log2 * svscale[sb * 128 + j] : a.c_log2) : -INFINITY;
         m_tile = fmaxf(m_tile, x[j]);
       }
       const bool grow = m_tile > m_ref + kRescaleLog2;
@@ -772,8 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_tile;
       }
       // P = 2^(x - m_ref) as bf16 pairs over the first 64 columns of the buffer
-      // (mixed caches: P times the value row's scale, split exactly into a
-      // bf16 high part in columns 0-63 and a bf16 low part in columns 64-127)
+      // (mixed caches: P times the value row's scale, as f16 pairs)
 #pragma unroll
       for (int j = 0; j < kT; ++j) {
         const float pj = m_ref == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
@@ -784,21 +797,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(x[hh * 64 + 2 * c], x[hh * 64 + 2 * c + 1]);
+        for (int c = 0; c < 32; ++c)
+          pk[c] = kE4M3 ? f16x2_bits(x[hh * 64 + 2 * c], x[hh * 64 + 2 * c + 1])
+                        : pack_bf16(x[hh * 64 + 2 * c], x[hh * 64 + 2 * c + 1]);
         tc::tmem_st32(tmem + lane_base + sb * 128 + hh * 32, pk);
-      }
-      if (kE4M3) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float a0 = x[hh * 64 + 2 * c], a1 = x[hh * 64 + 2 * c + 1];
-            pk[c] = pack_bf16(a0 - __bfloat162float(__float2bfloat16_rn(a0)),
-                              a1 - __bfloat162float(__float2bfloat16_rn(a1)));
-          }
-          tc::tmem_st32(tmem + lane_base + sb * 128 + 64 + hh * 32, pk);
-        }
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
@@ -978,21 +980,28 @@ int max_tiles(const csa_params& p, int Q, int64_t N, int mode, int64_t q_pos0) {
 
 // Split plan of the tensor-core path: one split per (query, half) for
 // multi-query launches; decode (one query per sequence) cuts the key list
-// into runs of kDecodeTiles tiles (more when that would exceed 16 runs), so
-// a CTA pipelines several tiles and writes one partial for them.  Depends on
-// Q and the key-list length only, never on the batch.
+// into runs of tiles (more per run when that would exceed 16 runs), so a CTA
+// pipelines several tiles and writes one partial for them.  Runs are 5 tiles
+// for lists up to 16 tiles (a CSA list of 1,152 keys: 5 + 4), 8 for longer
+// ones (raw-token and HCA lists: fewer, longer CTAs measured faster), and
+// mixed caches, whose CTAs spend longer per tile, split no list of up to 12
+// tiles.  Depends on Q, the key-list length and the cache format only, never
+// on the batch.
 constexpr int kDecodeTiles = 5;
+constexpr int kDecodeTilesLong = 8;
+constexpr int kDecodeTilesMixed = 12;
 
-void attend_tc_plan(const csa_params& p, int Q, int64_t N, int mode, int64_t q_pos0, int* splits,
-                    int* tps) {
+void attend_tc_plan(const csa_params& p, int Q, int64_t N, int mode, int64_t q_pos0, bool mixed,
+                    int* splits, int* tps) {
   const int nt = max_tiles(p, Q, N, mode, q_pos0);
-  if (Q > 1 || nt <= kDecodeTiles) {
+  const int run = mixed ? kDecodeTilesMixed : (nt > 16 ? kDecodeTilesLong : kDecodeTiles);
+  if (Q > 1 || nt <= run) {
     *splits = 1;
     *tps = nt > 0 ? nt : 1;
     return;
   }
   int t = (int)ceil_div(nt, 16);
-  if (t < kDecodeTiles) t = kDecodeTiles;
+  if (t < run) t = run;
   *tps = t;
   *splits = (int)ceil_div(nt, t);
 }
@@ -1002,7 +1011,7 @@ void attend_tc_plan(const csa_params& p, int Q, int64_t N, int mode, int64_t q_p
 // min(16, tiles of the longest list).
 size_t attend_tc_workspace(const csa_params& p, int Q, int64_t N, int mode, int64_t q_pos0) {
   int splits, tps;
-  attend_tc_plan(p, Q, N, mode, q_pos0, &splits, &tps);
+  attend_tc_plan(p, Q, N, mode, q_pos0, false, &splits, &tps);  // the most splits of either format
   if (splits <= 1) return 0;
   const int nt = max_tiles(p, Q, N, mode, q_pos0);
   splits = nt < 16 ? nt : 16;
@@ -1063,7 +1072,8 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.W = p.window;
   a.m = p.m;
   a.nc = p.D_qk / 64;
-  a.nsc = a.nc + (kv.dtype == CSA_E4M3 && mode != kAttendRawBlocks ? kv.nope / 64 : 0);
+  // mixed caches: each RoPE chunk takes two slots (high and low part)
+  a.nsc = a.nc + (kv.dtype == CSA_E4M3 && mode != kAttendRawBlocks ? a.nc - kv.nope / 64 : 0);
   a.nvc = p.D_v / 128;
   a.dense = mode == kAttendDense ? 1 : 0;
   a.rawblk = mode == kAttendRawBlocks ? 1 : 0;
@@ -1084,7 +1094,7 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   a.raw16 = reinterpret_cast<const uint16_t*>(raw.data);
   a.out = out;
   a.out_f32 = out_dtype == CSA_F32 ? 1 : 0;
-  attend_tc_plan(p, Q, N, mode, q_pos0, &a.splits, &a.tps);
+  attend_tc_plan(p, Q, N, mode, q_pos0, a.e4m3 != 0, &a.splits, &a.tps);
   // partials at the front of the workspace, (max, sum) pairs after them
   const size_t rows = (size_t)p.B * Q * p.H * a.splits;
   a.part = reinterpret_cast<float*>(ws);

@@ -97,8 +97,9 @@ class Step:
         else:
             kd = wl.k
         n_keys = ((kd + 3) // 4) * 4 + wl.W
-        if tc:  # decode splits the key list once it exceeds 5 tiles of 128 keys
-            attend = 1 + (1 if (wl.Q == 1 and -(-n_keys // 128) > 5) else 0)
+        if tc:  # decode splits a list of more than 5 tiles of 128 keys (mixed caches: 12)
+            run = 12 if wl.dtype == "mixed" else 5
+            attend = 1 + (1 if (wl.Q == 1 and -(-n_keys // 128) > run) else 0)
         else:
             attend = 1 + (1 if (rows < 1024 and kd + wl.W > 128) else 0)
         if wl.mode.startswith("hca"):
