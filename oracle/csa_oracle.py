@@ -52,6 +52,7 @@ import numpy as np
 
 __all__ = [
     "decode_bf16", "encode_bf16", "round_to_bf16", "decode_e4m3", "encode_e4m3",
+    "decode_e2m1", "encode_e2m1", "quantize_rows_e2m1", "dequantize_rows_e2m1",
     "round_to_f32", "quantize_rows_e4m3", "dequantize_rows_e4m3", "store_rows",
     "compress_weights", "compress", "n_vis", "index_scores", "index_scores_bf16", "topk_row",
     "topk",
@@ -156,6 +157,55 @@ def encode_e4m3(x: np.ndarray) -> np.ndarray:
     code = np.where(sub, code, ((en.astype(np.int64) + 7) << 3) | mn)
     sign = np.where(np.signbit(x), 0x80, 0)  # the sign survives rounding to zero
     return (code | sign).astype(np.uint8)
+
+
+def decode_e2m1(u4: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 codes (one per uint8, values 0..15) -> float64.
+
+    Layout s ee m, exponent bias 1, no infinities or NaN.  e == 0: subnormal
+    m * 0.5; otherwise (1 + m/2) * 2^(e-1): the magnitudes 0, 0.5, 1, 1.5, 2,
+    3, 4, 6.
+    """
+    b = np.asarray(u4, dtype=np.uint8).astype(np.int64) & 0xF
+    s = np.where(b & 0x8, -1.0, 1.0)
+    e = (b >> 1) & 0x3
+    m = b & 0x1
+    val = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.ldexp(1.0, e - 1))
+    return s * val
+
+
+def encode_e2m1(x: np.ndarray) -> np.ndarray:
+    """float64 -> E2M1 codes (one per uint8), round to nearest even, saturating
+    at +-6.  Spacing 0.5 below 2, 1 in [2, 4), 2 in [4, 6]; a tie goes to the
+    code with an even mantissa bit."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.minimum(np.abs(x), 6.0)
+    q = np.where(ax < 2.0, 0.5, np.where(ax < 4.0, 1.0, 2.0))
+    r = np.round(ax / q) * q  # round half to even on the grid: even multiples win
+    r = np.minimum(r, 6.0)
+    # magnitude -> code: 0, .5, 1, 1.5, 2, 3, 4, 6 -> 0..7
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    code = np.searchsorted(mags, r)
+    sign = np.where(np.signbit(x), 0x8, 0)
+    return (code | sign).astype(np.uint8)
+
+
+def quantize_rows_e2m1(v: np.ndarray) -> dict:
+    """FP4 storage of indexer-key rows ([csdn] section "V4 的其他升级": the
+    indexer's QK path is quantised to FP4 and dequantised to FP8 without
+    loss): one float32 scale per row, amax / 6 (1.0 for an all-zero row), and
+    each code the E2M1 rounding, taken directly from float64, of value /
+    scale.  Codes are returned one per uint8 (the cache packs two per byte)."""
+    v = np.asarray(v, dtype=np.float64)
+    amax = np.max(np.abs(v), axis=-1)
+    scale = np.where(amax > 0, amax / 6.0, 1.0).astype(np.float32)
+    codes = encode_e2m1(v / scale.astype(np.float64)[..., None])
+    return {"codes": codes, "scale": scale}
+
+
+def dequantize_rows_e2m1(codes, scale) -> np.ndarray:
+    """Exact float64 value of FP4 rows: code * scale."""
+    return decode_e2m1(codes) * np.asarray(scale, dtype=np.float64)[..., None]
 
 
 def round_to_f32(x: np.ndarray) -> np.ndarray:

@@ -562,3 +562,45 @@ def test_bf16_index_scores_are_torch_rounded_scores_and_ties_go_low():
     sel2 = O.topk(s16[:1], pos[:1], m, k2)[0]
     group = np.flatnonzero(s16[0, :N] == tie)
     assert group[0] in sel2 and not np.isin(group[1:], sel2).any()
+
+
+# ------------------------------------------------------------------ FP4 keys
+def test_e2m1_values_are_e4m3_values_and_the_format_extremes():
+    """Every E2M1 value converts to E4M3 without loss (the FP4 -> FP8 step of
+    the indexer keys; the E4M3 codec is pinned against torch above), the codes
+    0..7 increase from 0 through the smallest nonzero magnitude 0.5 to the
+    largest 6, and codes 8..15 are their negatives."""
+    c = np.arange(16, dtype=np.uint8)
+    v = O.decode_e2m1(c)
+    assert np.array_equal(O.decode_e4m3(O.encode_e4m3(v)), v)
+    assert np.all(np.diff(v[:8]) > 0) and v[0] == 0 and v[1] == 0.5 and v[7] == 6.0
+    assert np.array_equal(v[8:], -v[:8]) and np.signbit(v[8])
+
+
+def test_e2m1_encode_is_nearest_with_ties_to_even_by_brute_force():
+    g = np.random.default_rng(31)
+    x = np.concatenate([g.uniform(-7, 7, 20000), np.arange(-6.5, 6.75, 0.25)])
+    vals = O.decode_e2m1(np.arange(8, dtype=np.uint8))
+    code = O.encode_e2m1(x)
+    for xi, ci in zip(x, code):
+        ax = min(abs(xi), 6.0)
+        d = np.abs(vals - ax)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if best.size == 1 else [b for b in best if b % 2 == 0][0]
+        assert (ci & 7) == want, (xi, ci)
+        assert (ci >> 3) == (1 if np.signbit(xi) else 0)
+
+
+def test_e2m1_rows_round_trip_within_half_a_spacing_and_keep_the_row_max():
+    g = np.random.default_rng(32)
+    v = g.standard_normal((50, 128))
+    q = O.quantize_rows_e2m1(v)
+    back = O.dequantize_rows_e2m1(q["codes"], q["scale"])
+    s = q["scale"].astype(np.float64)[:, None]
+    spacing = np.where(np.abs(v) / s < 2, 0.5, np.where(np.abs(v) / s < 4, 1.0, 2.0)) * s
+    assert np.all(np.abs(back - v) <= spacing / 2 * (1 + 1e-6))
+    i = np.argmax(np.abs(v), axis=1)
+    r = np.arange(50)
+    np.testing.assert_allclose(np.abs(back[r, i]), np.abs(v[r, i]), rtol=1e-6)
+    # the row maximum takes the largest code magnitude (the scale is amax / 6)
+    assert np.all((q["codes"][r, i] & 7) == 7)
