@@ -381,6 +381,8 @@ def algorithmic_work(wl):
     # bytes of one stored entry / indexer key (mixed: e4m3 codes + fp32 scale, bf16 RoPE dims)
     entry_b = (wl.D_v + 4 + (wl.D_qk - wl.D_v) * 2) if mixed else wl.D_qk * esz
     key_b = (wl.d_I + 4) if mixed else wl.d_I * esz
+    if wl.keys == "e2m1":  # FP4 codes, two per byte, + fp32 scale
+        key_b = wl.d_I // 2 + 4
     qi_b = (wl.H_I * (wl.d_I + 4)) if mixed else wl.H_I * wl.d_I * esz
     decode = wl.mode.endswith("decode")
     new = N - (N - 1 if decode else 0)
@@ -592,6 +594,24 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne, dist, dev)
     units = job_units(wl, world)
     recall = None
+    if wl.keys == "e2m1":
+        # how much of the selection with the same keys in e4m3 the FP4 keys keep
+        # (the same draws; the keys quantised to e4m3 instead of FP4)
+        wl8 = wl.replace(keys="auto")
+        inp8 = synth.make_inputs(wl8, dev)
+        ref_step = Step(wl8, inp8)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            step.run(stream=stream)
+            ref_step.run(stream=stream)
+        torch.cuda.synchronize()
+        csa.device_status(stream)
+        a4, a8 = step.selected().cpu().numpy(), ref_step.selected().cpu().numpy()
+        hits = sum(np.intersect1d(a4[b, i], a8[b, i][a8[b, i] >= 0]).size
+                   for b in range(wl.B) for i in range(wl.Q))
+        recall = {"value": hits / int((a8 >= 0).sum()),
+                  "of": "the top-k sets with the same keys stored in e4m3", "sets": wl.B * wl.Q}
+        del ref_step, inp8
     if wl.scores == "bf16":
         # how much of the fp32-score selection the bf16-score selection keeps
         # (the same inputs, the step run once with each score dtype)
@@ -616,7 +636,7 @@ def measure(args, wl, dev, dist, world, rank, parts_wanted=True, e2e_steps=None,
            "cpu_baseline": cpu,
            "e2e": {"value": units / (e2e_ms / 1e3), "unit": "tok/s" if decode else "query-tok/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
-           "launches_per_step": step.launches_per_step(), "recall_vs_f32": recall}
+           "launches_per_step": step.launches_per_step(), "recall": recall}
     del step, step2, inp, inp2, g_full, g_full2, g_part, host_in, host_out
     gc.collect()
     torch.cuda.empty_cache()
@@ -924,7 +944,7 @@ def run_ours(args, wl):
                 "roofline": roofline(sw, r["per_part_ms"], r["ms"], peaks, peak_kind),
                 "e2e": r["e2e"], "gpu_launches": r["launches_per_step"] * steps,
                 "cpu_baseline": r["cpu_baseline"],
-                **({"recall_vs_f32": r["recall_vs_f32"]} if r.get("recall_vs_f32") else {})}
+                **({"recall": r["recall"]} if r.get("recall") else {})}
 
     prefill = None
     others = {}
@@ -933,7 +953,7 @@ def run_ours(args, wl):
         if not args.no_others:
             # the other rows of the path: HCA prefill and decode, mixed-precision decode
             for name in ("hca_prefill_1m", "hca_decode_1m", "csa_decode_fp8_512k",
-                         "csa_decode_raw_1m", "csa_decode_1m_bf16s"):
+                         "csa_decode_raw_1m", "csa_decode_1m_bf16s", "csa_decode_fp4_512k"):
                 others[name] = secondary(name, min(args.steps, 10))
             # a CSA layer and an HCA layer decoding token by token
             others["hybrid_decode_1m"] = measure_hybrid(args, synth.HYBRID["hybrid_decode_1m"],

@@ -54,7 +54,9 @@ typedef struct CUstream_st* csa_stream_t; /* == cudaStream_t */
 typedef enum {
   CSA_F32 = 0,  /* IEEE binary32 */
   CSA_BF16 = 1, /* bfloat16 */
-  CSA_E4M3 = 2  /* OCP FP8 E4M3 ("fn": no inf, NaN = 0x7f/0xff) with fp32 row scales */
+  CSA_E4M3 = 2, /* OCP FP8 E4M3 ("fn": no inf, NaN = 0x7f/0xff) with fp32 row scales */
+  CSA_E2M1 = 3  /* OCP FP4 E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives), two codes per
+                   byte, with fp32 row scales: indexer keys only */
 } csa_dtype;
 
 typedef enum {
@@ -76,6 +78,13 @@ typedef enum {
  *       one fp32 scale per row in `scale` [B, n_rows] (value = code * scale);
  *       the remaining width - nope channels (the RoPE dims) are bfloat16 in
  *       `rope` [B, n_rows, width - nope] (NULL when nope == width).
+ *   dtype E2M1 (FP4 indexer keys, [csdn] section "V4 的其他升级": the
+ *       indexer's QK path in FP4, turned into FP8 without loss): `data` is
+ *       [B, n_rows, width / 2] bytes, channel 2i in the low and channel 2i + 1
+ *       in the high four bits of byte i; one fp32 scale per row in `scale`
+ *       (value = code * scale); width even, nope == width, rope NULL.  Accepted
+ *       as the key cache of csa_index / csa_index_ex / csa_forward (with E4M3
+ *       q_idx) and as the output of csa_compress.
  */
 typedef struct {
   csa_dtype dtype;

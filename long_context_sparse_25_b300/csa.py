@@ -18,7 +18,7 @@ _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "libcsa_b300.so"
 HEADER = _PKG.parent / "include" / "csa.h"
 
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
 WS_TOPK, WS_ATTEND, WS_HCA, WS_FORWARD, WS_ATTEND_RAW = 0, 1, 2, 3, 4
 STALL_INDEX, STALL_ATTEND = 1, 2
 STATUS = {0: "CSA_OK", -1: "CSA_ERR_INVALID_ARG", -2: "CSA_ERR_UNSUPPORTED", -3: "CSA_ERR_ALIGNMENT",
@@ -115,6 +115,8 @@ def dtype_code(t: torch.Tensor) -> int:
         return BF16
     if t.dtype == torch.float8_e4m3fn:
         return E4M3
+    if t.dtype == torch.float4_e2m1fn_x2:  # two FP4 codes per byte
+        return E2M1
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -132,9 +134,11 @@ def _stream(stream=None):
 def rows(data: torch.Tensor, rope: torch.Tensor | None = None, scale: torch.Tensor | None = None,
          width: int | None = None) -> Rows:
     """Describe [B, n_rows, *] rows.  For e4m3 data the rope plane (bf16) and
-    the per-row fp32 scale are given separately; width = nope + rope width."""
+    the per-row fp32 scale are given separately; width = nope + rope width.
+    FP4 keys (torch.float4_e2m1fn_x2, two codes per byte) hold 2 * shape[-1]
+    channels, with their per-row scale."""
     dt = dtype_code(data)
-    nope = data.shape[-1]
+    nope = data.shape[-1] * (2 if dt == E2M1 else 1)
     if width is None:
         width = nope + (rope.shape[-1] if rope is not None else 0)
     return Rows(dt, _ptr(data), _ptr(rope), _ptr(scale), data.shape[-2], width, nope)

@@ -52,12 +52,20 @@ int check_ptr(const void* p, const char* name) {
   } while (0)
 
 int check_rows(const csa_rows* r, const char* name, int width, int64_t min_rows, bool allow_e4m3,
-               int e4m3_nope) {
+               int e4m3_nope, bool allow_e2m1) {
   if (!r) return fail(CSA_ERR_INVALID_ARG, "%s is NULL", name);
-  if (r->dtype != CSA_F32 && r->dtype != CSA_BF16 && r->dtype != CSA_E4M3)
+  if (r->dtype != CSA_F32 && r->dtype != CSA_BF16 && r->dtype != CSA_E4M3 &&
+      r->dtype != CSA_E2M1)
     return fail(CSA_ERR_UNSUPPORTED, "%s: unknown dtype %d", name, (int)r->dtype);
   if (r->dtype == CSA_E4M3 && !allow_e4m3)
     return fail(CSA_ERR_UNSUPPORTED, "%s: e4m3 rows are not accepted here", name);
+  if (r->dtype == CSA_E2M1) {
+    if (!allow_e2m1) return fail(CSA_ERR_UNSUPPORTED, "%s: e2m1 rows are not accepted here", name);
+    if (r->width % 2 != 0 || r->nope != r->width)
+      return fail(CSA_ERR_INVALID_ARG, "%s: e2m1 rows need an even width and nope == width", name);
+    if (!r->scale) return fail(CSA_ERR_INVALID_ARG, "%s.scale is NULL", name);
+    if (!aligned16(r->scale)) return fail(CSA_ERR_ALIGNMENT, "%s.scale is not 16-byte aligned", name);
+  }
   if (r->width != width)
     return fail(CSA_ERR_INVALID_ARG, "%s: width %d, expected %d", name, r->width, width);
   if (r->n_rows < min_rows)
@@ -179,7 +187,7 @@ int csa_compress(const void* x, const void* gate, csa_dtype in_dtype, const floa
   REQUIRE(s_begin >= 0 && s_end >= s_begin, CSA_ERR_INVALID_ARG, "bad entry range [%lld, %lld)",
           (long long)s_begin, (long long)s_end);
   REQUIRE(x_pos0 >= 0, CSA_ERR_INVALID_ARG, "x_pos0 < 0");
-  CHECK(check_rows(out, "out", C, s_end, true, -1));
+  CHECK(check_rows(out, "out", C, s_end, true, -1, true));
   if (s_end > s_begin) {
     CHECK_PTR(x);
     CHECK_PTR(gate);
@@ -206,11 +214,11 @@ int csa_index_ex(const csa_params* p, const void* q_idx, csa_dtype q_dtype, cons
           "scores must be F32 or BF16");
   CHECK(check_params(p, true, false));
   CHECK(check_positions(q_pos0, Q, N, p->m));
-  CHECK(check_rows(keys, "keys", p->d_I, N, true, p->d_I));
+  CHECK(check_rows(keys, "keys", p->d_I, N, true, p->d_I, true));
   REQUIRE(q_dtype == CSA_F32 || q_dtype == CSA_BF16 || q_dtype == CSA_E4M3, CSA_ERR_UNSUPPORTED,
           "unknown q_dtype");
-  REQUIRE((q_dtype == CSA_E4M3) == (keys->dtype == CSA_E4M3), CSA_ERR_UNSUPPORTED,
-          "q_idx and keys must both be e4m3 or both not");
+  REQUIRE((q_dtype == CSA_E4M3) == (keys->dtype == CSA_E4M3 || keys->dtype == CSA_E2M1),
+          CSA_ERR_UNSUPPORTED, "q_idx must be e4m3 exactly when the keys are e4m3 or e2m1");
   if (Q == 0 || N == 0) return ok();
   CHECK_PTR(q_idx);
   CHECK_PTR(w);
@@ -327,9 +335,9 @@ static int attend_common(const csa_params* p, const void* q, csa_dtype q_dtype, 
   REQUIRE(q_dtype == CSA_F32 || q_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED, "q must be F32 or BF16");
   REQUIRE(out_dtype == CSA_F32 || out_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
           "out must be F32 or BF16");
-  if (mode != kAttendRawBlocks) CHECK(check_rows(kv, "kv", p->D_qk, N, true, p->D_v));
+  if (mode != kAttendRawBlocks) CHECK(check_rows(kv, "kv", p->D_qk, N, true, p->D_v, false));
   if (p->window > 0 || mode == kAttendRawBlocks) {
-    CHECK(check_rows(raw, "raw", p->D_qk, 0, false, -1));
+    CHECK(check_rows(raw, "raw", p->D_qk, 0, false, -1, false));
     REQUIRE(raw_pos0 >= 0, CSA_ERR_INVALID_ARG, "raw_pos0 < 0");
     CHECK(check_window(p, raw, raw_pos0, q_pos0, Q));
   }
@@ -422,16 +430,16 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
   REQUIRE(ws && ws_bytes >= need, CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   REQUIRE(aligned16(ws), CSA_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   // validate every step before launching the first one
-  CHECK(check_rows(&a->kv, "kv", p->D_qk, N, true, p->D_v));
-  CHECK(check_rows(&a->keys, "keys", p->d_I, N, true, p->d_I));
-  CHECK(check_rows(&raw, "raw", p->D_qk, 0, false, -1));
+  CHECK(check_rows(&a->kv, "kv", p->D_qk, N, true, p->D_v, false));
+  CHECK(check_rows(&a->keys, "keys", p->d_I, N, true, p->d_I, true));
+  CHECK(check_rows(&raw, "raw", p->D_qk, 0, false, -1, false));
   // raw-token variant: the attention reads every raw row from raw_all
   csa_rows raw_all = raw;
   const int mode = a->raw_all ? kAttendRawBlocks : kAttendEntries;
   if (a->raw_all) {
     raw_all.data = const_cast<void*>(a->raw_all);
     raw_all.n_rows = a->raw_all_rows;
-    CHECK(check_rows(&raw_all, "raw_all", p->D_qk, 0, false, -1));
+    CHECK(check_rows(&raw_all, "raw_all", p->D_qk, 0, false, -1, false));
     REQUIRE(raw_all.dtype == CSA_BF16 || raw_all.dtype == CSA_F32, CSA_ERR_UNSUPPORTED,
             "raw_all must be F32 or BF16");
     CHECK(check_window(p, &raw_all, 0, a->q_pos0, a->Q));
@@ -459,8 +467,9 @@ int csa_forward(const csa_params* p, const csa_forward_args* a, void* ws, size_t
           "q must be F32 or BF16");
   REQUIRE(a->out_dtype == CSA_F32 || a->out_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
           "out must be F32 or BF16");
-  REQUIRE((a->q_idx_dtype == CSA_E4M3) == (a->keys.dtype == CSA_E4M3), CSA_ERR_UNSUPPORTED,
-          "q_idx and keys must both be e4m3 or both not");
+  REQUIRE((a->q_idx_dtype == CSA_E4M3) ==
+              (a->keys.dtype == CSA_E4M3 || a->keys.dtype == CSA_E2M1),
+          CSA_ERR_UNSUPPORTED, "q_idx must be e4m3 exactly when the keys are e4m3 or e2m1");
   if (a->q_idx_dtype == CSA_E4M3) CHECK_PTR(a->q_idx_scale);
   REQUIRE(a->score_dtype == CSA_F32 || a->score_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED,
           "score_dtype must be F32 or BF16");

@@ -20,6 +20,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
   return (float)v;
 }
 
+// FP4 E2M1 code (low four bits) -> fp32: s ee m, bias 1; the magnitudes
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_to_f32(uint8_t c) {
+  const int e = (c >> 1) & 3, m = c & 1;
+  const float mag = e == 0 ? 0.5f * (float)m : (1.f + 0.5f * (float)m) * (float)(1 << (e - 1));
+  return (c & 8) ? -mag : mag;
+}
+
 // Load element `i` of a row stored as fp32 / bf16 (e4m3 rows go through
 // RowView below, which also applies the row scale).
 __device__ __forceinline__ float load_elem(const void* base, csa_dtype dt, int64_t i) {
@@ -48,9 +56,13 @@ struct RowView {
   __device__ __forceinline__ int64_t row_index(int b, int64_t r) const {
     return (int64_t)b * n_rows + r;
   }
-  // Channel c of row (b, r) as fp32 (e4m3 codes multiplied by the row scale).
+  // Channel c of row (b, r) as fp32 (e4m3 / e2m1 codes multiplied by the row scale).
   __device__ __forceinline__ float get(int b, int64_t r, int c) const {
     int64_t ri = row_index(b, r);
+    if (dtype == CSA_E2M1) {
+      const uint8_t byte = reinterpret_cast<const uint8_t*>(data)[ri * (width / 2) + c / 2];
+      return e2m1_to_f32((uint8_t)((byte >> ((c & 1) * 4)) & 0xF)) * scale[ri];
+    }
     if (dtype == CSA_E4M3) {
       if (c < nope)
         return e4m3_to_f32(reinterpret_cast<const uint8_t*>(data)[ri * nope + c]) * scale[ri];

@@ -488,6 +488,57 @@ __global__ void __launch_bounds__(256) compress_e4m3_kernel(
   }
 }
 
+// FP4 E2M1 code of x (round to nearest, ties to the even mantissa bit,
+// saturating at +-6): the grid is 0.5 below 2, 1 in [2, 4), 2 in [4, 6].
+__device__ __forceinline__ uint32_t e2m1_code(double x) {
+  const double ax = fmin(fabs(x), 6.0);
+  const double q = ax < 2.0 ? 0.5 : (ax < 4.0 ? 1.0 : 2.0);
+  const double r = fmin(rint(ax / q) * q, 6.0);  // rint: half to even on the grid
+  // magnitude -> code: 0, .5, 1, 1.5 -> 0..3; 2, 3 -> 4, 5; 4, 6 -> 6, 7
+  const uint32_t mag = r < 2.0 ? (uint32_t)(r * 2.0) : (r < 4.0 ? (uint32_t)r + 2u : (uint32_t)(r * 0.5) + 4u);
+  return mag | (signbit(x) ? 8u : 0u);
+}
+
+// FP4 output (indexer keys): one block per entry; the pooled values in
+// double-float (exact in float64), the row scale amax / 6 rounded to fp32,
+// the codes decided in float64, two per byte.
+template <typename T>
+__global__ void __launch_bounds__(256) compress_e2m1_kernel(
+    const void* __restrict__ x, const void* __restrict__ g, const float* __restrict__ bias,
+    int64_t T_rows, int64_t row_off, int m, int C, int64_t s_begin, int64_t n_s,
+    uint8_t* __restrict__ codes, float* __restrict__ scale, int64_t out_rows) {
+  extern __shared__ double vals[];  // [C]
+  __shared__ double red[32];
+  const int64_t s = s_begin + blockIdx.x % n_s;
+  const int b = (int)(blockIdx.x / n_s);
+  const int64_t row0 = (int64_t)b * T_rows + s * m - row_off;
+  double amax = 0.0;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const ff pv = pool_ff<T>(x, g, bias, row0, C, m, c);
+    const double v = (double)pv.hi + (double)pv.lo;
+    vals[c] = v;
+    amax = fmax(amax, fabs(v));
+  }
+  for (int o = 16; o > 0; o >>= 1) amax = fmax(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double a = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0;
+    for (int o = 16; o > 0; o >>= 1) a = fmax(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (threadIdx.x == 0) red[0] = a;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float sc = amax > 0.0 ? __double2float_rn(amax / 6.0) : 1.0f;
+  const int64_t orow = (int64_t)b * out_rows + s;
+  if (threadIdx.x == 0) scale[orow] = sc;
+  for (int c2 = threadIdx.x; c2 < C / 2; c2 += blockDim.x) {
+    const uint32_t lo = e2m1_code(vals[2 * c2] / (double)sc);
+    const uint32_t hi = e2m1_code(vals[2 * c2 + 1] / (double)sc);
+    codes[orow * (C / 2) + c2] = (uint8_t)(lo | (hi << 4));
+  }
+}
+
 }  // namespace
 
 // Channels per thread: 4 fp32 / 8 bf16 (16-byte loads) unless the step has
@@ -540,6 +591,17 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
                             int64_t s_end, const csa_rows& out, cudaStream_t st) {
   const int64_t n_s = s_end - s_begin;
   if (n_s <= 0 || B <= 0) return cudaSuccess;
+  if (out.dtype == CSA_E2M1) {
+    const int64_t blocks = (int64_t)B * n_s;
+    const size_t smem = (size_t)C * sizeof(double);
+    if (in_dtype == CSA_F32)
+      compress_e2m1_kernel<float><<<(unsigned)blocks, 256, smem, st>>>(
+          x, gate, bias, T, x_pos0, m, C, s_begin, n_s, (uint8_t*)out.data, out.scale, out.n_rows);
+    else
+      compress_e2m1_kernel<uint16_t><<<(unsigned)blocks, 256, smem, st>>>(
+          x, gate, bias, T, x_pos0, m, C, s_begin, n_s, (uint8_t*)out.data, out.scale, out.n_rows);
+    return cudaGetLastError();
+  }
   if (out.dtype == CSA_E4M3) {
     const int64_t blocks = (int64_t)B * n_s;
     const size_t smem = (size_t)C * sizeof(double);
@@ -565,6 +627,7 @@ cudaError_t launch_compress_pair(const void* x0, const void* g0, const float* bi
                                  int64_t s_begin, int64_t s_end, cudaStream_t st) {
   const int64_t n_s = s_end - s_begin;
   const bool pair = out0.dtype != CSA_E4M3 && out1.dtype != CSA_E4M3 &&
+                    out0.dtype != CSA_E2M1 && out1.dtype != CSA_E2M1 &&
                     pool_vec(in_dtype, C0, B, n_s, m) == pool_vec(in_dtype, C1, B, n_s, m);
   if (n_s <= 0 || B <= 0) return cudaSuccess;
   if (!pair) {

@@ -25,7 +25,14 @@
 //               the scores.  They take alternate tiles (decode) or split the
 //               queries of an N = 256 tile (prefill).
 // Up to eight accumulators live in TMEM, so the MMA of a tile never waits for
-// the epilogue of an earlier one.  Every mbarrier wait is bounded; a timeout
+// the epilogue of an earlier one.
+//
+// FP4 keys ("一文搞懂 DeepSeek" section "V4 的其他升级": the indexer's QK path
+// in FP4, dequantised to FP8 without loss): the producer's TMA brings a tile
+// of packed E2M1 codes (half the bytes) into a staging buffer, two converter
+// warps turn every code into its E4M3 code (each E2M1 value is an E4M3 value)
+// in the 128-byte swizzled layout of the e4m3 stage, and the MMA and the
+// epilogue run as for e4m3 keys (the row scale is applied to the score).  Every mbarrier wait is bounded; a timeout
 // is recorded in a device error word (read by csa_device_status) and the
 // kernel returns.
 #include <cudaTypedefs.h>
@@ -54,6 +61,7 @@ struct TcArgs {
   int chunk_elems, n_chunks, ksteps;
   uint32_t tmem_cols;
   int stall;  // test aid: CTA 0's MMA issuer first waits on a flag that nothing sets
+  uint32_t stg_bytes;  // FP4 keys: bytes of a staged tile of codes
   const float* w;
   const float* q_scale;  // e4m3 only
   const float* k_scale;  // e4m3 only
@@ -147,8 +155,21 @@ __device__ __forceinline__ void issue_tile(uint32_t d, uint64_t ad, uint64_t bd,
   }
 }
 
-template <bool kFP8, int kEpiWG>
-__global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
+// Four E2M1 codes (the low four bits of each nibble of `nib4`, channel order
+// from the lowest nibble) -> four E4M3 codes, one per byte.  A byte permute
+// looks up the magnitude (0, 0.5, 1, 1.5 | 2, 3, 4, 6 as E4M3 bytes); the
+// sign bit moves to bit 7.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib4) {
+  const uint32_t mag = __byte_perm(0x3C383000u, 0x4C484440u, nib4 & 0x7777u);
+  const uint32_t sgn = ((nib4 & 0x8u) << 4) | ((nib4 & 0x80u) << 8) | ((nib4 & 0x800u) << 12) |
+                       ((nib4 & 0x8000u) << 16);
+  return mag | sgn;
+}
+
+constexpr int kConvWarps = 2;  // FP4 keys: warps converting staged codes to E4M3
+
+template <bool kFP8, int kEpiWG, bool kFP4>
+__global__ void __launch_bounds__(64 + 128 * kEpiWG + (kFP4 ? 32 * kConvWarps : 0), 1)
     index_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     const __grid_constant__ CUtensorMap tm_q, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -164,10 +185,18 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
   uint64_t* acc_full = b_empty + 2;
   uint64_t* acc_empty = acc_full + kMaxAcc;
   uint64_t* mma_done = acc_empty + kMaxAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* stg_full = mma_done + 1;  // FP4 keys: [stages] staged tile of codes landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_full + (kFP4 ? a.stages : 0));
+  uint8_t* sS = sB + (size_t)a.nb * a.b_bytes;  // FP4 keys: staging, moved past the barriers below
+  if (kFP4) {
+    sS = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 1023) & ~(uintptr_t)1023);
+  }
   // [epilogue warps][QPW * H_I], read as float4: 16-byte aligned
   float* a_w_smem = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~(uintptr_t)15);
+      (reinterpret_cast<uintptr_t>(kFP4 ? sS + (size_t)a.stages * a.stg_bytes
+                                        : reinterpret_cast<uint8_t*>(tmem_slot + 4)) + 15) &
+      ~(uintptr_t)15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NM = a.NQ * a.H_I;  // MMA N
@@ -175,8 +204,10 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
-      tc::mbar_init(&a_full[s], 1);
+      // FP4 keys: a stage is full once every converter warp has written it
+      tc::mbar_init(&a_full[s], kFP4 ? kConvWarps : 1);
       tc::mbar_init(&a_empty[s], 1);
+      if (kFP4) tc::mbar_init(&stg_full[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&b_full[s], 1);
@@ -220,17 +251,23 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
         }
         const uint32_t s = it % a.stages;
         if (!tc::mbar_wait(&a_empty[s], ((it / a.stages) & 1) ^ 1, err, 2)) break;
-        tc::mbar_expect_tx(&a_full[s], a.a_bytes);
         const int y = (int)((int64_t)b * a.n_rows + (int64_t)kt * kTileKeys);
-        for (int ch = 0; ch < a.n_chunks; ++ch)
-          tc::tma_load_2d(sA + s * a.a_bytes + ch * a.a_chunk_bytes, &tm_keys, &a_full[s],
-                          ch * a.chunk_elems, y);
+        if (kFP4) {
+          // the stage's MMA is done, so the converters are done with its staging too
+          tc::mbar_expect_tx(&stg_full[s], a.stg_bytes);
+          tc::tma_load_2d(sS + (size_t)s * a.stg_bytes, &tm_keys, &stg_full[s], 0, y);
+        } else {
+          tc::mbar_expect_tx(&a_full[s], a.a_bytes);
+          for (int ch = 0; ch < a.n_chunks; ++ch)
+            tc::tma_load_2d(sA + s * a.a_bytes + ch * a.a_chunk_bytes, &tm_keys, &a_full[s],
+                            ch * a.chunk_elems, y);
+        }
         ++it;
       }
       // let the loads this CTA issued land before it can exit (only matters
       // when a wait above gave up; otherwise the MMA issuer consumed them all)
       for (uint32_t j = it > (uint32_t)a.stages ? it - a.stages : 0; j < it; ++j)
-        tc::mbar_drain(&a_full[j % a.stages], (j / a.stages) & 1);
+        tc::mbar_drain(kFP4 ? &stg_full[j % a.stages] : &a_full[j % a.stages], (j / a.stages) & 1);
       for (uint32_t j = qcount > (uint32_t)a.nb ? qcount - a.nb : 0; j < qcount; ++j)
         tc::mbar_drain(&b_full[j % a.nb], (j / a.nb) & 1);
     }
@@ -289,6 +326,44 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG, 1)
       // every MMA issued must have completed before TMEM is released
       tc::mma_commit(mma_done);
       tc::mbar_drain(mma_done, 0);
+    }
+  } else if (kFP4 && warp >= 2 + 4 * kEpiWG) {
+    // ------------------------------------------------------------ converters
+    // Tile it: wait for its staged codes, write their E4M3 codes into the
+    // stage (each 16 bytes of codes -- 32 channels of one row -- become two
+    // 16-byte units of the row), make the writes visible to the tensor
+    // cores, then one arrival per warp on the stage's barrier.
+    const int ct = threadIdx.x - (64 + 128 * kEpiWG);
+    const int upr = a.d_I / 32;  // 16-byte units of codes per row
+    const int units = kTileKeys * upr;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && sch.next(b, qb, kt)) {
+      const uint32_t s = it % a.stages;
+      if (!tc::mbar_wait(&stg_full[s], (it / a.stages) & 1, err, 8)) { ok = false; break; }
+      const uint8_t* src = sS + (size_t)s * a.stg_bytes;
+      uint8_t* dst = sA + (size_t)s * a.a_bytes;
+      for (int u = ct; u < units; u += 32 * kConvWarps) {
+        const int r = u / upr, p = u - r * upr;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)u * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[2 * e] = e2m1x4_to_e4m3x4(w[e] & 0xffffu);
+          o[2 * e + 1] = e2m1x4_to_e4m3x4(w[e] >> 16);
+        }
+        // channels 32p .. 32p+31: chunk p / 4 of the row, units 2 (p % 4) and +1
+        uint8_t* crow = dst + (size_t)(p >> 2) * a.a_chunk_bytes + (size_t)r * 128;
+        const int u0 = (p & 3) * 2;
+        *reinterpret_cast<uint4*>(crow + (((u0) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(crow + (((u0 + 1) ^ (r & 7)) << 4)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&a_full[s]);
+      ++it;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -446,6 +521,21 @@ bool make_map(CUtensorMap* map, const void* base, bool fp8, int64_t rows, int co
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the packed FP4 key codes, [rows, bytes] uint8: a box of the
+// whole row (bytes <= 256, a multiple of 16) x box_rows, unswizzled.
+bool make_map_fp4(CUtensorMap* map, const void* base, int64_t rows, int bytes, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)bytes};
+  cuuint32_t box[2] = {(cuuint32_t)bytes, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int pow2_at_least(int x) {
   int p = 32;
   while (p < x) p <<= 1;
@@ -456,7 +546,7 @@ int pow2_at_least(int x) {
 
 bool index_tc_supported(const csa_params& p, csa_dtype q_dtype, const csa_rows& keys, int Q) {
   (void)Q;
-  const bool fp8 = keys.dtype == CSA_E4M3;
+  const bool fp8 = keys.dtype == CSA_E4M3 || keys.dtype == CSA_E2M1;
   if (fp8 != (q_dtype == CSA_E4M3)) return false;
   if (!fp8 && !(keys.dtype == CSA_BF16 && q_dtype == CSA_BF16)) return false;
   if (fp8 && keys.nope != keys.width) return false;
@@ -486,7 +576,8 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
                             const float* q_scale, const float* w, const csa_rows& keys,
                             int64_t q_pos0, int Q, int64_t N, void* scores, bool scores_bf16,
                             cudaStream_t st, bool fill_invisible) {
-  const bool fp8 = keys.dtype == CSA_E4M3;
+  const bool fp4 = keys.dtype == CSA_E2M1;         // staged, converted to E4M3
+  const bool fp8 = keys.dtype == CSA_E4M3 || fp4;  // e4m3 MMA
   (void)q_dtype;
   TcArgs a{};
   a.B = p.B;
@@ -522,8 +613,11 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   // weights and the query buffers (two when that still leaves 4 key stages).
   const size_t wbytes =
       (size_t)4 * epi_wg * (a.alt ? a.NQ : a.NQ / epi_wg) * p.H_I * sizeof(float);
-  const size_t fixed = 1024 + (5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 + wbytes;
-  const size_t per_stage = a.a_bytes + 2 * sizeof(uint64_t);
+  a.stg_bytes = fp4 ? (uint32_t)(kTileKeys * p.d_I / 2) : 0u;
+  const size_t fixed = 1024 + (5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 + wbytes +
+                       (fp4 ? 1024 : 0);
+  const size_t per_stage = a.a_bytes + 2 * sizeof(uint64_t) +
+                           (fp4 ? a.stg_bytes + sizeof(uint64_t) : 0);
   const size_t limit = 227 * 1024;
   auto stages_for = [&](int nb) {
     const size_t used = fixed + (size_t)nb * a.b_bytes;
@@ -555,8 +649,12 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   a.stall = take_debug_stall(kStallIndex) ? 1 : 0;
 
   CUtensorMap tm_keys, tm_q;
-  if (!make_map(&tm_keys, keys.data, fp8, (int64_t)p.B * keys.n_rows, p.d_I, kTileKeys))
+  if (fp4) {
+    if (!make_map_fp4(&tm_keys, keys.data, (int64_t)p.B * keys.n_rows, p.d_I / 2, kTileKeys))
+      return cudaErrorInvalidValue;
+  } else if (!make_map(&tm_keys, keys.data, fp8, (int64_t)p.B * keys.n_rows, p.d_I, kTileKeys)) {
     return cudaErrorInvalidValue;
+  }
   if (!make_map(&tm_q, q_idx, fp8, (int64_t)p.B * Q * p.H_I, p.d_I, NM)) return cudaErrorInvalidValue;
 
   int dev = 0, sms = 148;
@@ -566,21 +664,23 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   if (a.total < grid) grid = a.total;
   if (grid < 1) grid = 1;
   const size_t smem = 1024 + (size_t)a.stages * a.a_bytes + (size_t)a.nb * a.b_bytes +
-                      (2 * a.stages + 5 + 2 * kMaxAcc) * sizeof(uint64_t) + 16 + 16 +
-                      wbytes;
-  const int threads = 64 + 128 * epi_wg;
+                      (2 * a.stages + 5 + 2 * kMaxAcc + (fp4 ? a.stages : 0)) * sizeof(uint64_t) +
+                      16 + 16 + wbytes + (fp4 ? 1024 + (size_t)a.stages * a.stg_bytes : 0);
+  const int threads = 64 + 128 * epi_wg + (fp4 ? 32 * kConvWarps : 0);
   cudaError_t e;
-#define CSA_LAUNCH_TC(FP8, EW)                                                                  \
+#define CSA_LAUNCH_TC(FP8, EW, FP4)                                                             \
   do {                                                                                          \
-    e = cudaFuncSetAttribute(index_tc_kernel<FP8, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             (int)smem);                                                        \
+    e = cudaFuncSetAttribute(index_tc_kernel<FP8, EW, FP4>,                                     \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
     if (e != cudaSuccess) return e;                                                             \
-    index_tc_kernel<FP8, EW><<<(unsigned)grid, threads, smem, st>>>(tm_keys, tm_q, a);          \
+    index_tc_kernel<FP8, EW, FP4><<<(unsigned)grid, threads, smem, st>>>(tm_keys, tm_q, a);     \
   } while (0)
-  if (fp8) {
-    if (epi_wg == 2) CSA_LAUNCH_TC(true, 2); else CSA_LAUNCH_TC(true, 1);
+  if (fp4) {
+    CSA_LAUNCH_TC(true, 2, true);
+  } else if (fp8) {
+    if (epi_wg == 2) CSA_LAUNCH_TC(true, 2, false); else CSA_LAUNCH_TC(true, 1, false);
   } else {
-    if (epi_wg == 2) CSA_LAUNCH_TC(false, 2); else CSA_LAUNCH_TC(false, 1);
+    if (epi_wg == 2) CSA_LAUNCH_TC(false, 2, false); else CSA_LAUNCH_TC(false, 1, false);
   }
 #undef CSA_LAUNCH_TC
   e = cudaGetLastError();

@@ -25,6 +25,10 @@ Workloads (sizes from the pages' configurations):
   raw-token attention: the raw KV rows of all 2^20 positions are resident
   (``x_all``), and each query attends over the 4 raw tokens of each of its
   1024 selected blocks plus the window.
+* ``csa_decode_fp4_512k`` -- ``csa_decode_fp8_512k``'s shapes and seed with
+  the indexer keys stored in FP4 (E2M1 codes, two per byte, one fp32 scale
+  per row: amax / 6), and without the x20 outliers (a per-row FP4 scale would
+  flush the rest of such a row to zero; trained FP4 keys have none).
 * ``csa_decode_1m_bf16s`` -- ``csa_decode_1m`` (same inputs) with the indexer
   scores stored in bf16 and the top-k over those.
 * ``gproj_prefill_64k`` / ``gproj_decode_b32`` (``GPROJ``) -- the grouped
@@ -73,6 +77,7 @@ class Workload:
     softmax_scale: float | None = None
     attend: str = "entries"  # "entries" | "raw": the raw tokens of the selected blocks
     scores: str = "f32"      # dtype of the indexer scores: "f32" | "bf16"
+    keys: str = "auto"       # indexer-key cache: "auto" (as dtype) | "e2m1" (FP4, mixed only)
 
     @property
     def N(self) -> int:
@@ -124,6 +129,9 @@ WORKLOADS = {
     "csa_decode_raw_1m": Workload("csa_decode_raw_1m", "csa_decode", B=32, L=1 << 20, m=4, H=128,
                                   D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
                                   dtype="bf16", seed=2, attend="raw"),
+    "csa_decode_fp4_512k": Workload("csa_decode_fp4_512k", "csa_decode", B=64, L=1 << 19, m=4,
+                                    H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128,
+                                    Q=1, dtype="mixed", seed=4, outliers=0.0, keys="e2m1"),
     "csa_decode_1m_bf16s": Workload("csa_decode_1m_bf16s", "csa_decode", B=32, L=1 << 20, m=4,
                                     H=128, D_qk=576, D_v=512, H_I=64, d_I=128, k=1024, W=128, Q=1,
                                     dtype="bf16", seed=2, scores="bf16"),
@@ -185,6 +193,27 @@ def quantize_e4m3_rows(v: torch.Tensor, nope: int):
     return codes.contiguous(), scale.contiguous(), rope
 
 
+_E2M1_MAGS = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_e2m1_rows(v: torch.Tensor):
+    """(codes [.., d/2] as torch.float4_e2m1fn_x2 -- channel 2i in the low, 2i+1
+    in the high four bits of byte i --, scale f32 [..]): per-row scale
+    amax / 6 (1 for an all-zero row), codes the nearest E2M1 value of
+    value / scale (ties to the even code), saturating at 6."""
+    amax = v.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / 6.0, torch.ones_like(amax)).float()
+    x = v / scale.unsqueeze(-1)
+    ax = x.abs().clamp(max=6.0)
+    q = torch.where(ax < 2.0, 0.5, torch.where(ax < 4.0, 1.0, 2.0))
+    r = torch.minimum(torch.round(ax / q) * q, torch.tensor(6.0, device=v.device))
+    mags = torch.tensor(_E2M1_MAGS, device=v.device)
+    code = torch.searchsorted(mags, r.contiguous()).to(torch.uint8)
+    code = code | (torch.signbit(x).to(torch.uint8) << 3)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
+    return packed.view(torch.float4_e2m1fn_x2), scale.contiguous()
+
+
 def make_inputs(wl: Workload, device="cpu") -> dict:
     """All inputs of one workload as torch tensors on ``device``.
 
@@ -237,7 +266,9 @@ def make_inputs(wl: Workload, device="cpu") -> dict:
         if wl.mode.startswith("csa"):
             keys = _normal(wl, "keys", (B, N, wl.d_I), device, rms=wl.rmsnorm, outl="outl_keys")
             keys[:, N - 1].zero_()
-            if wl.dtype == "mixed":
+            if wl.keys == "e2m1":
+                inp["keys"], inp["keys_scale"] = quantize_e2m1_rows(keys)
+            elif wl.dtype == "mixed":
                 codes, scale, _ = quantize_e4m3_rows(keys, wl.d_I)
                 inp["keys"], inp["keys_scale"] = codes, scale
             else:

@@ -242,7 +242,8 @@ def store_rows(v: np.ndarray, dtype: str, nope: int | None = None) -> np.ndarray
     """Value the cache holds after storing float64 rows ``v`` in ``dtype``.
 
     'f32' and 'bf16' round each element to nearest even; 'e4m3' is the mixed
-    layout of ``quantize_rows_e4m3`` (``nope`` leading channels quantised).
+    layout of ``quantize_rows_e4m3`` (``nope`` leading channels quantised);
+    'e2m1' the FP4 rows of ``quantize_rows_e2m1``.
     """
     if dtype == "f64":
         return np.asarray(v, dtype=np.float64)
@@ -253,6 +254,9 @@ def store_rows(v: np.ndarray, dtype: str, nope: int | None = None) -> np.ndarray
     if dtype == "e4m3":
         q = quantize_rows_e4m3(v, v.shape[-1] if nope is None else nope)
         return dequantize_rows_e4m3(q["codes"], q["scale"], q["rope"])
+    if dtype == "e2m1":
+        q = quantize_rows_e2m1(v)
+        return dequantize_rows_e2m1(q["codes"], q["scale"])
     raise ValueError(dtype)
 
 

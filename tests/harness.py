@@ -37,6 +37,28 @@ def store_name(wl) -> str:
     return {"f32": "f32", "bf16": "bf16", "mixed": "e4m3"}[wl.dtype]
 
 
+def key_store_name(wl) -> str:
+    return "e2m1" if wl.keys == "e2m1" else store_name(wl)
+
+
+def unpack_e2m1(t: torch.Tensor) -> np.ndarray:
+    """FP4 codes, one per uint8, from a packed tensor (channel 2i in the low
+    four bits of byte i)."""
+    u = t.detach().cpu().contiguous().view(torch.uint8).numpy()
+    return np.stack([u & 15, u >> 4], axis=-1).reshape(*u.shape[:-1], u.shape[-1] * 2)
+
+
+def cached_keys_f64(wl, inp, b, rows=slice(None)) -> np.ndarray:
+    """Exact float64 values of the indexer-key cache rows of sequence b."""
+    if wl.keys == "e2m1":
+        return O.dequantize_rows_e2m1(unpack_e2m1(inp["keys"][b, rows]),
+                                      inp["keys_scale"][b, rows].cpu().numpy())
+    if wl.dtype == "mixed":
+        return O.dequantize_rows_e4m3(inp["keys"][b, rows].cpu().view(torch.uint8).numpy(),
+                                      inp["keys_scale"][b, rows].cpu().numpy())
+    return f64(inp["keys"][b, rows])
+
+
 class SeqOracle:
     """Oracle state of one sequence b of a workload: its caches after the
     step's compression, and per-query scores / selection / output."""
@@ -68,15 +90,11 @@ class SeqOracle:
             xi, gi = f64(inp["xi"][b]), f64(inp["gi"][b])
             new_keys = O.compress(xi[a:e], gi[a:e], f64(inp["bias_i"]), m)
             if decode:
-                if wl.dtype == "mixed":
-                    keys = O.dequantize_rows_e4m3(inp["keys"][b].cpu().view(torch.uint8).numpy(),
-                                                  inp["keys_scale"][b].cpu().numpy())
-                else:
-                    keys = f64(inp["keys"][b])
+                keys = cached_keys_f64(wl, inp, b)
             else:
                 keys = np.zeros((N, wl.d_I))
             keys = np.array(keys)
-            keys[n_cached:N] = O.store_rows(new_keys, store_name(wl), wl.d_I)
+            keys[n_cached:N] = O.store_rows(new_keys, key_store_name(wl), wl.d_I)
             self.keys = keys
             self.new_keys = keys[n_cached:N]
             qi = inp["q_idx"][b]

@@ -116,3 +116,23 @@ def test_group_proj_rejects_bad_arguments():
     assert f(FAKE, -1, 128, 512, FAKE, 8, 256, FAKE, csa.BF16, None) == -1
     # T = 0: nothing to do, no pointer needed, no launch
     assert f(None, 0, 128, 512, None, 8, 256, None, csa.BF16, None) == 0
+
+
+def test_fp4_key_rows_are_accepted_only_as_indexer_keys():
+    p = _p()
+    fp4 = csa.Rows(csa.E2M1, FAKE, None, FAKE, 100, 16, 16)
+    f = csa.lib.csa_index
+    # q_idx must be e4m3 with FP4 keys
+    assert f(C.byref(p), FAKE, csa.BF16, None, FAKE, C.byref(fp4), 0, 4, 100, FAKE, None) == -2
+    # odd width, missing scale
+    odd = csa.Rows(csa.E2M1, FAKE, None, FAKE, 100, 15, 15)
+    p15 = _p(d_I=15)
+    assert f(C.byref(p15), FAKE, csa.E4M3, FAKE, FAKE, C.byref(odd), 0, 4, 100, FAKE, None) == -1
+    noscale = csa.Rows(csa.E2M1, FAKE, None, None, 100, 16, 16)
+    assert f(C.byref(p), FAKE, csa.E4M3, FAKE, FAKE, C.byref(noscale), 0, 4, 100, FAKE, None) == -1
+    assert "scale" in csa.lib.csa_last_error().decode()
+    # not as attention rows
+    kv = csa.Rows(csa.E2M1, FAKE, None, FAKE, 100, 64, 64)
+    raw = _rows(64, n_rows=10)
+    assert csa.lib.csa_attend(C.byref(p), FAKE, csa.BF16, C.byref(kv), C.byref(raw), 50, FAKE, 53,
+                              1, 13, FAKE, csa.BF16, None, 0, None) == -2

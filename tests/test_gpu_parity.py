@@ -11,8 +11,8 @@ import oracle as O
 from long_context_sparse_25_b300 import csa, synth
 from long_context_sparse_25_b300.pipeline import Step
 
-from harness import (SeqOracle, check_out, check_scores, check_scores_bf16, check_selection,
-                     check_selection_bf16, f64)
+from harness import (SeqOracle, cached_keys_f64, check_out, check_scores, check_scores_bf16,
+                     check_selection, check_selection_bf16, f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +37,8 @@ CSA_CASES = {
     # indexer scores stored in bf16: decode (multi-CTA top-k over 16-bit keys)
     # and a prefill (one CTA per row)
     "decode_bf16_scores": (W["csa_decode_1m_bf16s"].replace(B=3, L=80000), None),
+    # FP4 indexer keys converted to FP8 in the indexer (a multi-CTA top-k row)
+    "decode_fp4_keys": (W["csa_decode_fp4_512k"].replace(B=2, L=80004), None),
     "prefill_bf16_scores_ragged": (W["csa_prefill_64k"].replace(L=2051, Q=2051, k=32,
                                                                 scores="bf16"), 160),
     "prefill_raw_8k": (W["csa_prefill_64k"].replace(L=8192, Q=8192, attend="raw"), 24),
@@ -81,8 +83,7 @@ def test_csa_forward_matches_oracle(case, cuda_device):
             got_kv = O.dequantize_rows_e4m3(inp["kv_nope"][b, n0:].cpu().view(torch.uint8).numpy(),
                                             inp["kv_scale"][b, n0:].cpu().numpy(),
                                             inp["kv_rope"][b, n0:].cpu().view(torch.int16).numpy().view(np.uint16))
-            got_keys = O.dequantize_rows_e4m3(inp["keys"][b, n0:].cpu().view(torch.uint8).numpy(),
-                                              inp["keys_scale"][b, n0:].cpu().numpy())
+            got_keys = cached_keys_f64(wl, inp, b, slice(n0, None))
         else:
             kvt = inp["kv"] if decode else step.kv_buf
             kt = inp["keys"] if decode else step.keys_buf
