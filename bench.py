@@ -985,6 +985,8 @@ def run_ours(args, wl):
         "prefill": prefill,
         "others": others or None,
     }
+    if head.get("recall"):
+        line["recall"] = head["recall"]
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
