@@ -133,7 +133,14 @@ def _seq_inputs(wl, inp, b):
         for k in ("xi", "gi", "w"):
             d[k] = _f64(inp[k][b])
         d["bias_i"] = _f64(inp["bias_i"])
-        if wl.dtype == "mixed":
+        if wl.keys == "e2m1":  # FP4 codes, two per byte
+            import numpy as np
+            import oracle as O
+            u = inp["keys"][b].cpu().view(torch.uint8).numpy()
+            codes = np.stack([u & 15, u >> 4], axis=-1).reshape(u.shape[0], -1)
+            d["keys"] = O.dequantize_rows_e2m1(codes, inp["keys_scale"][b].cpu().numpy())
+            d["q_idx"] = _f64(inp["q_idx"][b]) * inp["q_idx_scale"][b].cpu().double().numpy()[..., None]
+        elif wl.dtype == "mixed":
             d["keys"] = _f64(inp["keys"][b]) * inp["keys_scale"][b].cpu().double().numpy()[:, None]
             d["q_idx"] = _f64(inp["q_idx"][b]) * inp["q_idx_scale"][b].cpu().double().numpy()[..., None]
         else:
@@ -159,7 +166,7 @@ def _oracle_decode_step(wl, d):
         return O.hca_attend(d["q"], kv, d["x"], wl.raw_pos0, pos, m, wl.W, wl.D_v, wl.scale)
     keys = np.array(d["keys"])
     keys[N - 1] = O.store_rows(O.compress(d["xi"][a:a + m], d["gi"][a:a + m], d["bias_i"], m),
-                               store)[0]
+                               "e2m1" if wl.keys == "e2m1" else store)[0]
     scores = O.index_scores(d["q_idx"], d["w"], keys, pos, m)
     sel = O.topk(scores, pos, m, wl.k)
     return O.csa_attend(d["q"], kv, d["x"], wl.raw_pos0, sel, pos, wl.W, wl.D_v, wl.scale)

@@ -13,7 +13,10 @@
 //
 // Tiles: 128 tokens x 256 features per tile (one M = 128, N = 256 MMA per
 // 16-element K step), 64-element K blocks (one 128-byte swizzle atom) per ring
-// stage: 16 KB of o and 32 KB of w, loaded by two TMA boxes.  Persistent CTAs
+// stage: 16 KB of o and 32 KB of w, loaded by two TMA boxes.  When those tiles
+// would leave most SMs idle (a decode step: one block of tokens), the tiles
+// are 128 x 64 with eight 24 KB stages, so the weight stream spreads over
+// every SM.  Persistent CTAs
 // (one per SM) take tiles in (group, token block, feature block) order with
 // the feature block fastest, so the CTAs working at the same time share each
 // token block's rows of o in L2, and a group's 16 MB of weights stay in L2
@@ -22,8 +25,8 @@
 // Roles: warp 0 TMA producer (one thread), warp 1 TMEM allocator and MMA
 // issuer (one thread; descriptors advanced by constant offsets), warps 2-5
 // epilogue (tcgen05.ld of the accumulator, bf16 / fp32 conversion, stores).
-// Two accumulators of 256 columns fill the 512 TMEM columns, so the MMAs of a
-// tile run while the epilogue drains the previous one.  Every mbarrier wait
+// Two accumulators (of 256 or 64 columns) in TMEM, so the MMAs of a tile run
+// while the epilogue drains the previous one.  Every mbarrier wait
 // is bounded; a timeout is recorded in a device error word (read by
 // csa_device_status) and the kernel returns after its copies and MMAs in
 // flight have landed.
@@ -39,13 +42,20 @@ namespace {
 __device__ int g_gproj_error = 0;
 
 constexpr int kBM = 128;                       // tokens per tile
-constexpr int kBN = 256;                       // features per tile
 constexpr int kBK = 64;                        // K elements per stage (128 bytes)
 constexpr uint32_t kABytes = kBM * 128;        // 16 KB
-constexpr uint32_t kBBytes = kBN * 128;        // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
+
+// Features per tile: 256 (a prefill: many token blocks) or 64 (a decode step:
+// one token block, so narrow tiles spread the weight stream over every SM),
+// with the stage count that keeps about 192 KB of operands in flight.
+template <int BN>
+struct Tile {
+  static constexpr int kBN = BN;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN == 256 ? 4 : 8;
+};
 
 struct GpArgs {
   int64_t T;
@@ -65,9 +75,13 @@ __device__ __forceinline__ void tile_coords(const GpArgs& a, int64_t tile, int& 
   g = (int)(r / a.n_mb);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gproj_tc_kernel(const __grid_constant__ CUtensorMap tm_o,
                     const __grid_constant__ CUtensorMap tm_w, const GpArgs a) {
+  constexpr int kBN = Tile<BN>::kBN;
+  constexpr uint32_t kStageBytes = Tile<BN>::kStageBytes;
+  constexpr int kStages = Tile<BN>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -96,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tmap(&tm_o);
     tc::prefetch_tmap(&tm_w);
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * kBN < 32 ? 32 : 2 * kBN);
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, 512);
+    tc::tmem_dealloc(tmem_base, 2 * kBN < 32 ? 32 : 2 * kBN);
   }
 }
 
@@ -279,7 +293,11 @@ cudaError_t launch_group_proj(const void* o, int64_t T, int H, int D_v, const vo
   a.K = (H / G) * D_v;
   a.nkb = a.K / kBK;
   a.n_mb = (int)((T + kBM - 1) / kBM);
-  a.n_nb = d_g / kBN;
+  // narrow tiles when the wide ones would leave most SMs idle
+  const int64_t wide_tiles = (int64_t)G * a.n_mb * (d_g / 256);
+  const bool narrow = wide_tiles < num_sms() / 2;
+  const int BN = narrow ? 64 : 256;
+  a.n_nb = d_g / BN;
   a.n_tiles = (int64_t)G * a.n_mb * a.n_nb;
   a.y_ld = (int64_t)G * d_g;
   a.out_f32 = y_f32 ? 1 : 0;
@@ -287,15 +305,20 @@ cudaError_t launch_group_proj(const void* o, int64_t T, int H, int D_v, const vo
   if (a.n_tiles == 0) return cudaSuccess;
   CUtensorMap tm_o, tm_w;
   if (!make_map(&tm_o, o, T, (int64_t)H * D_v, (int64_t)H * D_v, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&tm_w, w, (int64_t)G * d_g, a.K, a.K, kBN)) return cudaErrorInvalidValue;
-  const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * sizeof(uint64_t) + 16;
-  cudaError_t e = cudaFuncSetAttribute(gproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
+  if (!make_map(&tm_w, w, (int64_t)G * d_g, a.K, a.K, BN)) return cudaErrorInvalidValue;
   int64_t grid = num_sms();
   if (a.n_tiles < grid) grid = a.n_tiles;
-  gproj_tc_kernel<<<(unsigned)grid, kThreads, smem, st>>>(tm_o, tm_w, a);
-  return cudaGetLastError();
+  auto launch = [&](auto tile) -> cudaError_t {
+    using T = decltype(tile);
+    const size_t smem =
+        1024 + (size_t)T::kStages * T::kStageBytes + (2 * T::kStages + 5) * sizeof(uint64_t) + 16;
+    cudaError_t e = cudaFuncSetAttribute(gproj_tc_kernel<T::kBN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gproj_tc_kernel<T::kBN><<<(unsigned)grid, kThreads, smem, st>>>(tm_o, tm_w, a);
+    return cudaGetLastError();
+  };
+  return narrow ? launch(Tile<64>{}) : launch(Tile<256>{});
 }
 
 }  // namespace csa
