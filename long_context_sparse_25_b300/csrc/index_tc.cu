@@ -625,9 +625,9 @@ cudaError_t launch_index_tc(const csa_params& p, const void* q_idx, csa_dtype q_
   };
   a.nb = stages_for(2) >= 4 ? 2 : 1;
   int stages = stages_for(a.nb);
-  // about 128 KB of key tiles in flight per SM keeps HBM busiest (more only
-  // queues up)
-  const int cap = (int)((128 * 1024) / a.a_bytes);
+  // about 128 KB of key tiles in flight per SM keeps HBM busiest with 32 KB
+  // bf16 tiles (more only queues up); the 16 KB e4m3 tiles take 192 KB
+  const int cap = (int)(((fp8 ? 192 : 128) * 1024) / a.a_bytes);
   if (stages > (cap > 4 ? cap : 4)) stages = cap > 4 ? cap : 4;
   if (stages < 2) return cudaErrorNotSupported;
   a.stages = stages;
