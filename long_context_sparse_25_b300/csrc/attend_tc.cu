@@ -235,6 +235,37 @@ __device__ __forceinline__ MixUnit mix_load(const AttArgs& a, int64_t row, bool 
   return r;
 }
 
+// A code chunk unit of row pointer sp (the unit's bytes in chunk 0: codes of
+// an entry, or bf16 values of a window row) for chunk c.
+__device__ __forceinline__ MixUnit mix_load_code(const uint8_t* sp, bool win, int c) {
+  MixUnit r;
+  r.inv = 1.f;
+  r.kind = win ? 0 : 1;
+  if (win) {
+    r.v = __ldg(reinterpret_cast<const uint4*>(sp + c * 128));
+  } else {
+    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(sp + c * 64));
+    r.v = make_uint4(cv.x, cv.y, 0u, 0u);
+  }
+  return r;
+}
+
+// Eight e4m3 codes (byte i = code i) as eight f16 values, exactly (every
+// e4m3 value is an f16 value).
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 w) {
+  uint4 o;
+  asm("{\n\t.reg .b16 a0, a1, a2, a3;\n\t"
+      "mov.b32 {a0, a1}, %4;\n\t"
+      "mov.b32 {a2, a3}, %5;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, a1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %2, a2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %3, a3;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+      : "r"(w.x), "r"(w.y));
+  return o;
+}
+
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -248,13 +279,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint4 mix_f16(const MixUnit& r) {
   uint32_t o[4];
   if (r.kind == 1) {
-    const uint32_t w2[2] = {r.v.x, r.v.y};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-          (__nv_fp8x2_storage_t)((w2[e >> 1] >> ((e & 1) * 16)) & 0xffffu), __NV_E4M3);
-      o[e] = (uint32_t)h.x | ((uint32_t)h.y << 16);
-    }
+    return e4m3x8_to_f16x8(make_uint2(r.v.x, r.v.y));
   } else {
     const uint32_t w4[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
 #pragma unroll
@@ -428,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SlotSrc s0, s1;
         int tma;    // bf16 caches: 1 = 128 consecutive entry rows, 2 = 128 consecutive
         int tma_y;  //   raw rows (from tma_y), loaded by one TMA box per chunk; 0 = gathered
+        bool code_only;  // mixed caches: no window row among the warp's units
       };
       auto issue_chunk = [&](int c, const TileRows& t) -> bool {
         int okw = 1;
@@ -458,14 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
-              raw[i] = mix_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7);
+              raw[i] = mix_load_code(t.sp[i], (t.wb >> i) & 1, c);
           }
 #pragma unroll
           for (int i = 0; i < kUnits; ++i) {
             const int unit = pt + kProd * i;
             if (unit < (int)(kChunk / 16))
-              *reinterpret_cast<uint4*>(sRing + pslot * kChunk + swz(unit >> 3, unit & 7)) =
-                  mix_f16(raw[i]);
+              *reinterpret_cast<uint4*>(sRing + pslot * kChunk + dso[i]) = mix_f16(raw[i]);
           }
           tc::fence_proxy_async_smem();
           tc::mbar_arrive(&ring_full[pslot]);
@@ -481,6 +506,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           pslot = 0;
           pph ^= 1;
         }
+        return true;
+      };
+      // Mixed caches: two code chunks per round (c0 of rows t0, c1 of rows t1)
+      // into the next two slots.  A producer thread's loads of a chunk wait
+      // one memory latency, so it keeps two chunks' loads in flight, issued
+      // before the slots are known to be free.
+      auto issue_code2 = [&](int c0, const TileRows& t0, int c1, const TileRows& t1) -> bool {
+        const uint32_t s0 = pslot, p0 = pph;
+        const uint32_t s1 = pslot + 1 == kRing ? 0 : pslot + 1;
+        const uint32_t p1 = s1 == 0 ? pph ^ 1 : pph;
+        auto wait_slots = [&]() -> bool {
+          int okw = 1;
+          if (lane == 0)
+            okw = tc::mbar_wait(&ring_empty[s0], p0 ^ 1, err, 11) &&
+                  tc::mbar_wait(&ring_empty[s1], p1 ^ 1, err, 11);
+          return __shfl_sync(0xffffffffu, okw, 0) != 0;
+        };
+        if (t0.code_only && t1.code_only) {
+          // codes only (warp-uniform): 8 bytes per unit, widened in registers
+          uint2 v0[kUnits], v1[kUnits];
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i)
+            if (i < kUnits - 1 || last_unit) {
+              v0[i] = __ldg(reinterpret_cast<const uint2*>(t0.sp[i] + c0 * 64));
+              v1[i] = __ldg(reinterpret_cast<const uint2*>(t1.sp[i] + c1 * 64));
+            }
+          if (!wait_slots()) return false;
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i)
+            if (i < kUnits - 1 || last_unit) {
+              *reinterpret_cast<uint4*>(sRing + s0 * kChunk + dso[i]) = e4m3x8_to_f16x8(v0[i]);
+              *reinterpret_cast<uint4*>(sRing + s1 * kChunk + dso[i]) = e4m3x8_to_f16x8(v1[i]);
+            }
+        } else {
+          MixUnit raw0[kUnits], raw1[kUnits];
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i)
+            if (i < kUnits - 1 || last_unit) {
+              raw0[i] = mix_load_code(t0.sp[i], (t0.wb >> i) & 1, c0);
+              raw1[i] = mix_load_code(t1.sp[i], (t1.wb >> i) & 1, c1);
+            }
+          if (!wait_slots()) return false;
+#pragma unroll
+          for (int i = 0; i < kUnits; ++i)
+            if (i < kUnits - 1 || last_unit) {
+              *reinterpret_cast<uint4*>(sRing + s0 * kChunk + dso[i]) = mix_f16(raw0[i]);
+              *reinterpret_cast<uint4*>(sRing + s1 * kChunk + dso[i]) = mix_f16(raw1[i]);
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&ring_full[s0]);
+        tc::mbar_arrive(&ring_full[s1]);
+        pslot = s1 + 1 == kRing ? 0 : s1 + 1;
+        pph = pslot == 0 ? p1 ^ 1 : p1;
         return true;
       };
       // Mixed caches: the high and the low part of RoPE chunk c (over the row
@@ -559,8 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool win = (v >> 63) != 0;
           t.rr[i] = row;
           t.wb |= (win ? 1u : 0u) << i;
-          t.sp[i] = (win ? rawb : kvb) + row * rowb + (lane & 7) * 16;
+          t.sp[i] = win ? rawb + row * rowb + (lane & 7) * 16
+                  : (kE4M3 ? a.codes + row * a.nope + (lane & 7) * 8
+                           : kvb + row * rowb + (lane & 7) * 16);
         }
+        t.code_only = kE4M3 && __all_sync(0xffffffffu, t.wb == 0);
         t.tma = 0;
         t.tma_y = 0;
         if (!kE4M3) {
@@ -612,12 +694,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           // QK^T chunks: the nc chunks in order; mixed caches' RoPE chunks as
           // (high, low) pairs
           const int ncode = kE4M3 ? a.nope / 64 : a.nc;
-          for (int c = 0; c < ncode && ok; ++c) ok = issue_chunk(c, cur);
+          if (kE4M3) {
+            int c = 0;
+            for (; c + 1 < ncode && ok; c += 2) ok = issue_code2(c, cur, c + 1, cur);
+            if (c < ncode && ok) ok = issue_chunk(c, cur);
+          } else {
+            for (int c = 0; c < ncode && ok; ++c) ok = issue_chunk(c, cur);
+          }
           if (kE4M3)
             for (int c = ncode; c < a.nc && ok; ++c) ok = issue_pair(c, cur);
         }
         if (u >= 1)
-          for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, prev);
+          if (kE4M3) {
+            int c = 0;
+            for (; c + 1 < a.nvc && ok; c += 2) ok = issue_code2(vc0 + c, prev, vc0 + c + 1, prev);
+            if (c < a.nvc && ok) ok = issue_chunk(vc0 + c, prev);
+          } else {
+            for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, prev);
+          }
         prev = cur;
         if (u + 1 < n) tile_rows(u + 1, wnext, cur);
       }
