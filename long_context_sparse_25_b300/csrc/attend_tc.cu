@@ -214,27 +214,6 @@ struct MixUnit {
   int kind;
 };
 
-__device__ __forceinline__ MixUnit mix_load(const AttArgs& a, int64_t row, bool win, int c,
-                                            int uc) {
-  MixUnit r;
-  r.inv = 1.f;
-  const int d0 = c * 64 + uc * 8;
-  if (win) {  // a raw (window) row: bf16 values
-    r.kind = 0;
-    r.v = __ldg(reinterpret_cast<const uint4*>(a.raw16 + row * a.D_qk + d0));
-  } else if (d0 >= a.nope) {  // RoPE dims of an entry
-    r.kind = 0;
-    const int rw = a.D_qk - a.nope;
-    r.v = __ldg(reinterpret_cast<const uint4*>(a.rope + row * rw + (d0 - a.nope)));
-    r.inv = 1.f / __ldg(a.kscale + row);
-  } else {  // codes of an entry
-    r.kind = 1;
-    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(a.codes + row * a.nope + d0));
-    r.v = make_uint4(cv.x, cv.y, 0u, 0u);
-  }
-  return r;
-}
-
 // A code chunk unit of row pointer sp (the unit's bytes in chunk 0: codes of
 // an entry, or bf16 values of a window row) for chunk c.
 __device__ __forceinline__ MixUnit mix_load_code(const uint8_t* sp, bool win, int c) {
@@ -342,9 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = mask_empty + 2;  // [2]
   uint64_t* mma_done = o_done + 2;
   uint64_t* q_conv = mma_done + 1;  // e4m3: Q converted to f16 by every producer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_conv + 1);
+  uint64_t* row_full = q_conv + 1;   // the tile's row table written
+  uint64_t* row_empty = row_full + 1;  // ... and read by every producer warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(row_empty + 1);
   uint32_t* smask = tmem_slot + 4;  // [2][4] ballot words of the tile's valid slots
   float* svscale = reinterpret_cast<float*>(smask + 8);  // e4m3: [2][128] row scales of the tile
+  uint32_t* srow = reinterpret_cast<uint32_t*>(svscale + 256);  // [128] row | window << 31
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = &g_attend_tc_error;
@@ -379,6 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&o_done[1], 1);
     tc::mbar_init(mma_done, 1);
     tc::mbar_init(q_conv, kProd);
+    tc::mbar_init(row_full, kProdWarps);
+    tc::mbar_init(row_empty, kProdWarps);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tm_q);
     if (!kE4M3) {
@@ -447,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unit in chunk 0; mixed caches: the row and its kind), and the two mask
       // slots of each thread
       struct TileRows {
-        int64_t rr[kUnits];
+        uint32_t rr[kUnits];  // the rows (fewer than 2^31 in all)
         const uint8_t* sp[kUnits];
         uint32_t wb;
         SlotSrc s0, s1;
@@ -563,30 +547,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // Mixed caches: the high and the low part of RoPE chunk c (over the row
-      // scale) go to two consecutive slots from one load.
+      // scale) go to two consecutive slots from one load.  Every unit's value
+      // and scale loads are issued first, without branches (a window row
+      // reads scale 0 and takes 1), so that no load waits for the division
+      // of an earlier unit; then the slots are waited for.
       auto issue_pair = [&](int c, const TileRows& t) -> bool {
         const uint32_t s0 = pslot, p0 = pph;
         const uint32_t s1 = pslot + 1 == kRing ? 0 : pslot + 1;
         const uint32_t p1 = s1 == 0 ? pph ^ 1 : pph;
+        const int d0 = c * 64 + (lane & 7) * 8;  // unit & 7 == lane & 7
+        const int rw = a.D_qk - a.nope;
+        uint4 rv[kUnits];
+        float ks[kUnits];
+#pragma unroll
+        for (int i = 0; i < kUnits; ++i)
+          if (i < kUnits - 1 || last_unit) {
+            const bool win = (t.wb >> i) & 1;
+            const int64_t row = t.rr[i];
+            const uint16_t* src = win ? a.raw16 + row * a.D_qk + d0 : a.rope + row * rw + (d0 - a.nope);
+            rv[i] = __ldg(reinterpret_cast<const uint4*>(src));
+            ks[i] = __ldg(a.kscale + (win ? 0 : row));
+          }
         int okw = 1;
         if (lane == 0)
           okw = tc::mbar_wait(&ring_empty[s0], p0 ^ 1, err, 11) &&
                 tc::mbar_wait(&ring_empty[s1], p1 ^ 1, err, 11);
         okw = __shfl_sync(0xffffffffu, okw, 0);
         if (!okw) return false;
-        MixUnit raw[kUnits];
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
-          const int unit = pt + kProd * i;
-          if (unit < (int)(kChunk / 16))
-            raw[i] = mix_load(a, t.rr[i], (t.wb >> i) & 1, c, unit & 7);
-        }
-#pragma unroll
-        for (int i = 0; i < kUnits; ++i) {
-          const int unit = pt + kProd * i;
-          if (unit < (int)(kChunk / 16)) {
+          if (i < kUnits - 1 || last_unit) {
+            MixUnit r;
+            r.v = rv[i];
+            r.kind = 0;
+            r.inv = ((t.wb >> i) & 1) ? 1.f : 1.f / ks[i];
             uint4 hi, lo;
-            mix_f16_pair(raw[i], hi, lo);
+            mix_f16_pair(r, hi, lo);
             *reinterpret_cast<uint4*>(sRing + s0 * kChunk + dso[i]) = hi;
             *reinterpret_cast<uint4*>(sRing + s1 * kChunk + dso[i]) = lo;
           }
@@ -598,50 +594,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         pph = pslot == 0 ? p1 ^ 1 : p1;
         return true;
       };
-      // A warp's units of a chunk cover 44 key rows (unit i of lane L is row
-      // 4 warp + 12 i + L/8, shared by 8 lanes): lane L looks up rows q = L
-      // and q = L + 32 of that list and the lanes exchange them by shuffles.
-      // Key-list words are fetched a tile ahead: those two rows, then the two
-      // mask slots pt and pt + 96.
+      // The tile's 128 key rows go through a table in shared memory: thread
+      // pt resolves slots pt and pt + 96 (which it needs for the softmax's
+      // masks anyway) and writes them; after every producer has, it reads the
+      // rows of its own units (unit i: row pt/8 + 12 i).  row_full / row_empty
+      // (one arrival per producer warp) order the writes of a table against
+      // the reads of the one before it.  Key-list words are fetched a tile
+      // ahead.
       struct TileWords {
-        int32_t w[4];
+        int32_t w[2];
       };
       const bool has1 = pt + kProd < kT;
-      auto unit_row = [&](int q) -> int { return 4 * warp + 12 * (q >> 2) + (q & 3); };
-      const int q1 = lane, q2 = lane + 32;
-      const bool has_q2 = q2 < 4 * kUnits;
       auto tile_words = [&](int u, TileWords& t) {
         const int jt = (tile0 + u) * kT;
-        const int r1 = unit_row(q1), r2 = unit_row(q2);
-        t.w[0] = r1 < kT ? slot_word(a, kl, qrow, jt + r1) : 0;
-        t.w[1] = (has_q2 && r2 < kT) ? slot_word(a, kl, qrow, jt + r2) : 0;
-        t.w[2] = slot_word(a, kl, qrow, jt + pt);
-        t.w[3] = slot_word(a, kl, qrow, jt + (has1 ? pt + kProd : pt));
+        t.w[0] = slot_word(a, kl, qrow, jt + pt);
+        t.w[1] = slot_word(a, kl, qrow, jt + (has1 ? pt + kProd : pt));
       };
-      auto tile_rows = [&](int u, const TileWords& tw, TileRows& t) {
+      int tbl = 0;  // tables written so far
+      auto tile_rows = [&](int u, const TileWords& tw, TileRows& t) -> bool {
         const int jt = (tile0 + u) * kT;
-        // (row | win << 63) of this lane's two rows of the warp's list
-        auto packed = [&](int r, int32_t word) -> unsigned long long {
-          const SlotSrc ss = slot_src(a, kl, b, jt + (r < kT ? r : 0), word);
-          return (unsigned long long)ss.row | ((unsigned long long)(ss.win ? 1 : 0) << 63);
-        };
-        const unsigned long long v1 = packed(unit_row(q1), tw.w[0]);
-        const unsigned long long v2 = has_q2 ? packed(unit_row(q2), tw.w[1]) : 0ull;
+        t.s0 = slot_src(a, kl, b, jt + pt, tw.w[0]);
+        t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[1]);
+        // every warp has read the previous table
+        if (tbl > 0 && !tc::mbar_wait(row_empty, (tbl - 1) & 1, err, 14)) return false;
+        srow[pt] = (uint32_t)t.s0.row | (t.s0.win ? 0x80000000u : 0u);
+        if (has1) srow[pt + kProd] = (uint32_t)t.s1.row | (t.s1.win ? 0x80000000u : 0u);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(row_full);
+        if (!tc::mbar_wait(row_full, tbl & 1, err, 15)) return false;
         t.wb = 0;
 #pragma unroll
         for (int i = 0; i < kUnits; ++i) {
-          const int src = 4 * i + (lane >> 3);
-          const unsigned long long a1 = __shfl_sync(0xffffffffu, v1, src & 31);
-          const unsigned long long a2 = __shfl_sync(0xffffffffu, v2, src & 31);
-          const unsigned long long v = src < 32 ? a1 : a2;
-          const int64_t row = (int64_t)(v & ~(1ull << 63));
-          const bool win = (v >> 63) != 0;
-          t.rr[i] = row;
+          const int r = (i < kUnits - 1 || last_unit) ? (pt >> 3) + (kProd / 8) * i : 0;
+          const uint32_t v = srow[r];
+          const int64_t row = (int64_t)(v & 0x7fffffffu);
+          const bool win = (v >> 31) != 0;
+          t.rr[i] = (uint32_t)row;
           t.wb |= (win ? 1u : 0u) << i;
           t.sp[i] = win ? rawb + row * rowb + (lane & 7) * 16
                   : (kE4M3 ? a.codes + row * a.nope + (lane & 7) * 8
                            : kvb + row * rowb + (lane & 7) * 16);
         }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(row_empty);
+        ++tbl;
         t.code_only = kE4M3 && __all_sync(0xffffffffu, t.wb == 0);
         t.tma = 0;
         t.tma_y = 0;
@@ -659,13 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             t.tma_y = (int)((int64_t)b * a.raw_rows + (kl.lo - a.raw_pos0) + (jt - kl.k_ent));
           }
         }
-        t.s0 = slot_src(a, kl, b, jt + pt, tw.w[2]);
-        t.s1 = slot_src(a, kl, b, jt + (has1 ? pt + kProd : pt), tw.w[3]);
+        return true;
       };
       TileRows cur, prev;
       TileWords wnext;
       tile_words(0, wnext);
-      tile_rows(0, wnext, cur);
+      ok = ok && tile_rows(0, wnext, cur);
       for (int u = 0; u <= n && ok; ++u) {
         if (u + 1 < n) tile_words(u + 1, wnext);  // in flight during this tile's issues
         if (u < n) {
@@ -682,15 +677,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             smask[(u & 1) * 4 + warp] = bal0;
             if (warp == 0) smask[(u & 1) * 4 + 3] = bal1;
           }
+          // mixed caches: the value rows' scales load while the QK^T chunks
+          // are issued; the words are published after them (the softmax
+          // needs them only once S is complete)
+          float ksv0 = 1.f, ksv1 = 1.f;
           if (kE4M3) {
-            svscale[(u & 1) * 128 + pt] =
-                (cur.s0.valid && !cur.s0.win) ? __ldg(a.kscale + cur.s0.row) : 1.f;
-            if (has1)
-              svscale[(u & 1) * 128 + pt + kProd] =
-                  (cur.s1.valid && !cur.s1.win) ? __ldg(a.kscale + cur.s1.row) : 1.f;
+            if (cur.s0.valid && !cur.s0.win) ksv0 = __ldg(a.kscale + cur.s0.row);
+            if (has1 && cur.s1.valid && !cur.s1.win) ksv1 = __ldg(a.kscale + cur.s1.row);
+          } else {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
           }
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&mask_full[u & 1]);
           // QK^T chunks: the nc chunks in order; mixed caches' RoPE chunks as
           // (high, low) pairs
           const int ncode = kE4M3 ? a.nope / 64 : a.nc;
@@ -701,8 +698,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             for (int c = 0; c < ncode && ok; ++c) ok = issue_chunk(c, cur);
           }
-          if (kE4M3)
+          if (kE4M3) {
             for (int c = ncode; c < a.nc && ok; ++c) ok = issue_pair(c, cur);
+            svscale[(u & 1) * 128 + pt] = ksv0;
+            if (has1) svscale[(u & 1) * 128 + pt + kProd] = ksv1;
+            __syncwarp();
+            if (lane == 0 && ok) tc::mbar_arrive(&mask_full[u & 1]);
+          }
         }
         if (u >= 1)
           if (kE4M3) {
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < a.nvc && ok; ++c) ok = issue_chunk(vc0 + c, prev);
           }
         prev = cur;
-        if (u + 1 < n) tile_rows(u + 1, wnext, cur);
+        if (u + 1 < n && ok) ok = tile_rows(u + 1, wnext, cur);
       }
       // every copy must land before the CTA can exit: this thread's cp.async
       // (their arrivals on the ring barriers happen by themselves), and (pt 0)
@@ -1200,6 +1202,9 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   memset(&tm_raw, 0, sizeof(tm_raw));
   if (!make_map_bf16(&tm_q, q, (int64_t)p.B * Q * p.H, p.D_qk, 128)) return cudaErrorInvalidValue;
   // bf16 caches: dense runs of entry rows and window rows load as 128-row boxes
+  // the producers pass rows around as 31-bit indices
+  if ((int64_t)p.B * kv.n_rows > 0x7fffffff || (int64_t)p.B * raw.n_rows > 0x7fffffff)
+    return cudaErrorInvalidValue;
   if (!a.e4m3) {
     if (!make_map_bf16(&tm_kv, kv.data, (int64_t)p.B * kv.n_rows, p.D_qk, 128))
       return cudaErrorInvalidValue;
@@ -1210,7 +1215,8 @@ cudaError_t launch_attend_tc(const csa_params& p, const void* q, const csa_rows&
   const int64_t grid = (int64_t)p.B * Q * 2 * a.splits;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = 1024 + (size_t)a.nc * kChunk + (size_t)kRing * kChunk +
-                      (2 * kRing + 12 + kMaxQChunks) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float);
+                      (2 * kRing + 14 + kMaxQChunks) * sizeof(uint64_t) + 16 + 32 + 2 * 128 * sizeof(float) +
+                      128 * sizeof(uint32_t);
   cudaError_t e;
   if (a.e4m3) {
     e = cudaFuncSetAttribute(attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
