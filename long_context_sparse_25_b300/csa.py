@@ -153,8 +153,9 @@ def workspace_size(p: Params, which: int, Q: int, N: int) -> int:
 
 
 def topk_launches(p: Params, Q: int, N: int) -> int:
-    """Kernels one csa_topk call launches for these sizes."""
-    return 1
+    """Kernels one csa_topk call launches for these sizes: three (sample,
+    filter, final) for a few long rows, one otherwise."""
+    return 3 if (N > 16384 and p.k <= 4096 and p.B * Q < 256) else 1
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
