@@ -77,26 +77,33 @@ __device__ __forceinline__ int tiles_visible(const TcArgs& a, int qb) {
   return (int)((nv + kTileKeys - 1) / kTileKeys);
 }
 
-// The (b, qb, kt) tiles of one CTA, in the same order for every role.
+// The (b, qb, kt) tiles of one CTA, in the same order for every role.  The
+// sizes it walks by are copied into the struct (registers): read through a
+// pointer to the kernel's parameters they were generic loads of parameter
+// space on every tile, a few hundred cycles of the MMA issuer's loop.
 struct Sched {
-  const TcArgs* a;
-  int c, G;
+  int mode, tps, nQB, B, c, G;
+  int64_t total;
   int64_t t, t_end;  // mode 0
   int64_t r;         // mode 1: round
   int b, qb, kt, kt_end;
 
   __device__ void init(const TcArgs& args, int cta, int grid) {
-    a = &args;
+    mode = args.mode;
+    tps = args.tps;
+    nQB = args.nQB;
+    B = args.B;
+    total = args.total;
     c = cta;
     G = grid;
-    if (args.mode == 0) {
-      t = args.total * cta / grid;
-      t_end = args.total * (cta + 1) / grid;
+    if (mode == 0) {
+      t = total * cta / grid;
+      t_end = total * (cta + 1) / grid;
       // position of tile t, then walked forward without divisions
-      const int64_t per_b = (int64_t)args.nQB * args.tps;
+      const int64_t per_b = (int64_t)nQB * tps;
       b = (int)(t / per_b);
-      qb = (int)((t / args.tps) % args.nQB);
-      kt = (int)(t % args.tps);
+      qb = (int)((t / tps) % nQB);
+      kt = (int)(t % tps);
     } else {
       r = 0;
       kt = 0;
@@ -104,16 +111,16 @@ struct Sched {
     }
   }
 
-  __device__ bool next(int& ob, int& oqb, int& okt) {
-    if (a->mode == 0) {
+  __device__ bool next(const TcArgs& args, int& ob, int& oqb, int& okt) {
+    if (mode == 0) {
       if (t >= t_end) return false;
       ob = b;
       oqb = qb;
       okt = kt;
       ++t;
-      if (++kt == a->tps) {
+      if (++kt == tps) {
         kt = 0;
-        if (++qb == a->nQB) {
+        if (++qb == nQB) {
           qb = 0;
           ++b;
         }
@@ -124,12 +131,12 @@ struct Sched {
       // zig-zag over units ordered from the heaviest (latest queries) down
       int64_t p = r * G + ((r & 1) ? (G - 1 - c) : c);
       ++r;
-      if (p >= a->total) return false;
-      int64_t u = a->total - 1 - p;
-      qb = (int)(u / a->B);
-      b = (int)(u % a->B);
+      if (p >= total) return false;
+      int64_t u = total - 1 - p;
+      qb = (int)(u / B);
+      b = (int)(u % B);
       kt = 0;
-      kt_end = tiles_visible(*a, qb);
+      kt_end = tiles_visible(args, qb);
     }
     ob = b;
     oqb = qb;
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG + (kFP4 ? 32 * kConvWarps : 
       // ---------------------------------------------------------- producer
       uint32_t it = 0, qcount = 0;
       int pb = -1, pqb = -1;
-      while (sch.next(b, qb, kt)) {
+      while (sch.next(a, b, qb, kt)) {
         if (b != pb || qb != pqb) {
           const uint32_t bi = qcount % a.nb;
           if (!tc::mbar_wait(&b_empty[bi], ((qcount / a.nb) & 1) ^ 1, err, 1)) break;
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG + (kFP4 ? 32 * kConvWarps : 
       bool ok = true;
       // test aid: the producer's first loads are in flight while this waits
       if (a.stall && blockIdx.x == 0) ok = tc::flag_wait(&g_index_never_set, tc::kStallNs, err, 7);
-      while (ok && sch.next(b, qb, kt)) {
+      while (ok && sch.next(a, b, qb, kt)) {
         if (b != pb || qb != pqb) {
           if (qcount > 0) tc::mma_commit(&b_empty[(qcount - 1) % a.nb]);
           bi = qcount % a.nb;
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG + (kFP4 ? 32 * kConvWarps : 
     const int units = kTileKeys * upr;
     uint32_t it = 0;
     bool ok = true;
-    while (ok && sch.next(b, qb, kt)) {
+    while (ok && sch.next(a, b, qb, kt)) {
       const uint32_t s = it % a.stages;
       if (!tc::mbar_wait(&stg_full[s], (it / a.stages) & 1, err, 8)) { ok = false; break; }
       const uint8_t* src = sS + (size_t)s * a.stg_bytes;
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(64 + 128 * kEpiWG + (kFP4 ? 32 * kConvWarps : 
     int cur_b = -1, cur_qb = -1;
     int64_t nv_q[4] = {0, 0, 0, 0};  // visible entries of this warpgroup's queries
     uint32_t tile_i = 0;
-    while (sch.next(b, qb, kt)) {
+    while (sch.next(a, b, qb, kt)) {
       if (a.alt && (int)(tile_i++ & 1) != wg) {  // the other warpgroup's tile
         ++acc_it;
         continue;
