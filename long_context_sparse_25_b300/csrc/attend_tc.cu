@@ -26,9 +26,12 @@
 // keys x 64 dims.  For
 // every tile of 128 keys three producer warps gather the D_qk/64 chunks of the
 // keys and then, one tile later, the D_v/128 chunks of the value half, with
-// 16-byte cp.async copies: each lane computes its own gathered row address
-// and swizzled destination (TMA gathers take their operands from warp-uniform
-// registers, so 32 lanes with 32 different rows serialise).  Each thread's
+// 16-byte cp.async copies.  The tile's 128 rows go through a table in shared
+// memory: each producer thread resolves two slots of the key list and writes
+// their rows, then reads the rows of its own units; each lane computes its
+// own gathered addresses and swizzled destinations (TMA gathers take their
+// operands from warp-uniform registers, so 32 lanes with 32 different rows
+// serialise).  Each thread's
 // copies of a chunk arrive on the chunk's barrier by themselves once they
 // have landed (cp.async.mbarrier.arrive), so the producers run ahead as far
 // as the ring allows; the MMA issuer, after its wait, issues the proxy fence
@@ -40,7 +43,10 @@
 // and the row scale moves out of the keys: the tile holds S'_j = q_nope .
 // code_j + q_rope . (rope_j / c_j), the RoPE dims over the row scale split
 // exactly into an f16 high and low part (two ring slots that meet the same Q
-// chunk), and the softmax takes S_j = c_j S'_j.  P . V runs on the codes with
+// chunk), and the softmax takes S_j = c_j S'_j.  These chunks pass through
+// the producers' registers: a thread issues the 8-byte code loads of two
+// chunks before it waits for their ring slots, and every value and scale
+// load of the RoPE chunk before its two slots.  P . V runs on the codes with
 // c_j folded into P, rounded once to f16.  Q is converted to f16 in shared
 // memory once per CTA.  The MMA order is S(0), S(1), PV(0), S(2), PV(1), ...
 // so the softmax of tile u overlaps S(u+1).  A key row doubles as its value

@@ -15,8 +15,9 @@
 // (N = 256) so that each key tile read from L2 feeds 4x more MMA work.
 //
 // Roles (warp-specialised, one CTA per SM, persistent):
-//   warp 0      TMA producer: key tiles into a ring of stages (about 128 KB
-//               in flight), query blocks into one or two B buffers;
+//   warp 0      TMA producer: key tiles into a ring of stages (128 KB of
+//               32 KB bf16 tiles, 192 KB of 16 KB e4m3 tiles in flight),
+//               query blocks into one or two B buffers;
 //   warp 1      TMEM allocator and MMA issuer (one thread; descriptors are
 //               advanced by constant offsets in an unrolled K loop, and the
 //               next stage's and accumulator's barriers are probed ahead);
