@@ -445,10 +445,13 @@ __global__ void __launch_bounds__(256) compress_kernel(const CJob j0, const CJob
                      n_s);
 }
 
-// Mixed e4m3 + bf16 output: one block per entry; the pooled values in
-// double-float (exact in float64), then the row scale and the codes in float64.
+// Mixed e4m3 + bf16 output: one block per entry, one thread per channel (the
+// double-float pool of a channel is a long dependent chain: a thread that
+// took three of them made a decode step's compress three chains long); the
+// pooled values in double-float (exact in float64), then the row scale and
+// the codes in float64.
 template <typename T>
-__global__ void __launch_bounds__(256) compress_e4m3_kernel(
+__global__ void __launch_bounds__(1024) compress_e4m3_kernel(
     const void* __restrict__ x, const void* __restrict__ g, const float* __restrict__ bias,
     int64_t T_rows, int64_t row_off, int m, int C, int nope, int64_t s_begin, int64_t n_s,
     uint8_t* __restrict__ codes, uint16_t* __restrict__ rope, float* __restrict__ scale,
@@ -499,11 +502,11 @@ __device__ __forceinline__ uint32_t e2m1_code(double x) {
   return mag | (signbit(x) ? 8u : 0u);
 }
 
-// FP4 output (indexer keys): one block per entry; the pooled values in
-// double-float (exact in float64), the row scale amax / 6 rounded to fp32,
-// the codes decided in float64, two per byte.
+// FP4 output (indexer keys): one block per entry, one thread per channel; the
+// pooled values in double-float (exact in float64), the row scale amax / 6
+// rounded to fp32, the codes decided in float64, two per byte.
 template <typename T>
-__global__ void __launch_bounds__(256) compress_e2m1_kernel(
+__global__ void __launch_bounds__(1024) compress_e2m1_kernel(
     const void* __restrict__ x, const void* __restrict__ g, const float* __restrict__ bias,
     int64_t T_rows, int64_t row_off, int m, int C, int64_t s_begin, int64_t n_s,
     uint8_t* __restrict__ codes, float* __restrict__ scale, int64_t out_rows) {
@@ -540,6 +543,13 @@ __global__ void __launch_bounds__(256) compress_e2m1_kernel(
 }
 
 }  // namespace
+
+// Threads of a one-block-per-entry kernel: one per channel, whole warps, at
+// most 1024 (wider rows loop).
+static int entry_threads(int C) {
+  const int t = (C + 31) / 32 * 32;
+  return t > 1024 ? 1024 : (t < 32 ? 32 : t);
+}
 
 // Channels per thread: 4 fp32 / 8 bf16 (16-byte loads) unless the step has
 // few entries (a decode step): then one channel per thread, so that the rare
@@ -595,10 +605,10 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
     const int64_t blocks = (int64_t)B * n_s;
     const size_t smem = (size_t)C * sizeof(double);
     if (in_dtype == CSA_F32)
-      compress_e2m1_kernel<float><<<(unsigned)blocks, 256, smem, st>>>(
+      compress_e2m1_kernel<float><<<(unsigned)blocks, entry_threads(C), smem, st>>>(
           x, gate, bias, T, x_pos0, m, C, s_begin, n_s, (uint8_t*)out.data, out.scale, out.n_rows);
     else
-      compress_e2m1_kernel<uint16_t><<<(unsigned)blocks, 256, smem, st>>>(
+      compress_e2m1_kernel<uint16_t><<<(unsigned)blocks, entry_threads(C), smem, st>>>(
           x, gate, bias, T, x_pos0, m, C, s_begin, n_s, (uint8_t*)out.data, out.scale, out.n_rows);
     return cudaGetLastError();
   }
@@ -606,11 +616,11 @@ cudaError_t launch_compress(const void* x, const void* gate, csa_dtype in_dtype,
     const int64_t blocks = (int64_t)B * n_s;
     const size_t smem = (size_t)C * sizeof(double);
     if (in_dtype == CSA_F32)
-      compress_e4m3_kernel<float><<<(unsigned)blocks, 256, smem, st>>>(
+      compress_e4m3_kernel<float><<<(unsigned)blocks, entry_threads(C), smem, st>>>(
           x, gate, bias, T, x_pos0, m, C, out.nope, s_begin, n_s, (uint8_t*)out.data,
           (uint16_t*)out.rope, out.scale, out.n_rows);
     else
-      compress_e4m3_kernel<uint16_t><<<(unsigned)blocks, 256, smem, st>>>(
+      compress_e4m3_kernel<uint16_t><<<(unsigned)blocks, entry_threads(C), smem, st>>>(
           x, gate, bias, T, x_pos0, m, C, out.nope, s_begin, n_s, (uint8_t*)out.data,
           (uint16_t*)out.rope, out.scale, out.n_rows);
     return cudaGetLastError();
