@@ -139,11 +139,14 @@ def test_topk_bit_exact_on_oracle_scores(cuda_device):
     """csa_topk fed fp32 scores (with many exact ties, signed zeros, -inf
     beyond visibility) returns exactly the oracle's index lists."""
     rng = np.random.default_rng(5)
-    # rows held in registers (N <= 16384; N % 4 != 0 takes scalar loads), long
-    # rows over several CTAs, rows shorter than k, and a row of all-equal scores
+    # rows held in shared memory, long rows over several CTAs (16-byte score
+    # loads; N % 4 != 0 takes the scalar filter; visible lengths that end
+    # inside a 4-score group), rows shorter than k, and a row of all-equal
+    # scores
     for (B, Q, N, k, m, q_pos0) in [(2, 37, 700, 64, 4, 2700), (1, 5, 20000, 1024, 4, 79999),
                                      (3, 9, 300, 1024, 4, 1000), (1, 300, 16384, 1024, 4, 65235),
-                                     (2, 7, 1001, 256, 4, 3998)]:
+                                     (2, 7, 1001, 256, 4, 3998), (1, 3, 20001, 1024, 4, 80003),
+                                     (1, 4, 20000, 1024, 4, 70000)]:
         s = rng.standard_normal((B, Q, N))
         s = np.where(rng.uniform(size=s.shape) < 0.3, np.round(s, 1), s)  # ties
         s = np.where(rng.uniform(size=s.shape) < 0.05, 0.0, s)
@@ -170,7 +173,8 @@ def test_topk_bit_exact_on_oracle_bf16_scores(cuda_device):
     rng = np.random.default_rng(11)
     for (B, Q, N, k, m, q_pos0) in [(2, 37, 700, 64, 4, 2700), (1, 5, 20000, 1024, 4, 79999),
                                      (3, 9, 300, 1024, 4, 1000), (2, 3, 262144, 1024, 4, 1048575),
-                                     (2, 7, 1001, 256, 4, 3998)]:
+                                     (2, 7, 1001, 256, 4, 3998), (1, 3, 20003, 512, 4, 80011),
+                                     (1, 4, 20000, 1024, 4, 70000)]:
         s = rng.standard_normal((B, Q, N))
         s = np.where(rng.uniform(size=s.shape) < 0.05, 0.0, s)
         s = np.where(rng.uniform(size=s.shape) < 0.05, -0.0, s)
