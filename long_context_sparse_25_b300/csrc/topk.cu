@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const ST* __restrict
 //              row, in index order (ballots), into a list of the (key, index)
 //              composites of its keys >= tau;
 //   C  final:  one CTA per row; if at least kk keys reached tau the kk largest
-//              of the row are all among them: the warps copy the lists into
+//              of the row are all among them: the lists are copied into
 //              shared memory, a radix select on their keys (12-bit digits)
 //              gives the key T of the kk-th largest and how many keys equal to
 //              T are needed, and one pass over the candidates (already in
@@ -541,17 +541,22 @@ __global__ void __launch_bounds__(1024) topk_final_kernel(const ST* __restrict__
   };
   const bool in_smem = nc <= kCandSmem;
   if (in_smem) {
-    // warp w copies lists w, w + 32, ... (each contiguous in cand) by
-    // cp.async, all of them in flight at once
-    const int lane = threadIdx.x & 31;
-    for (int l = threadIdx.x >> 5; l < L; l += 32) {
+    // the lists (each contiguous in cand) copied by cp.async, all of them in
+    // flight at once: a warp per list when they are long, a thread per list
+    // when they are short (few rows split into many slices: up to 4096 lists
+    // of a few candidates each)
+    auto copy = [&](int l, int e0, int step) {
       const int o = off[l], c = off[l + 1] - o;
-      if (c == 0) continue;
       const unsigned long long* src = lr.cand + row * N + list_start(l);
-      for (int e = lane; e < c; e += 32) {
+      for (int e = e0; e < c; e += step) {
         const uint32_t dst = (uint32_t)__cvta_generic_to_shared(cbuf + o + e);
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src + e) : "memory");
       }
+    };
+    if (nc >= 16 * L) {
+      for (int l = threadIdx.x >> 5; l < L; l += 32) copy(l, threadIdx.x & 31, 32);
+    } else {
+      for (int l = threadIdx.x; l < L; l += blockDim.x) copy(l, 0, 1);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
