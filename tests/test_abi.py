@@ -95,6 +95,26 @@ def test_workspace_query_and_forward_workspace_check():
     assert csa.lib.csa_forward(C.byref(p), C.byref(a), FAKE, 16, None) == -4
 
 
+def test_topk_workspace_covers_the_long_row_scratch():
+    """The top-k workspace: nothing for rows the one-CTA-per-row path takes
+    (N <= 16384, or 256 rows and more, or k > 4096); for a few long rows, room
+    for one 8-byte (key, index) candidate per score, the per-row threshold and
+    the per-list counts (at most 256 slices x 16 lists per row), each region
+    rounded up to 256 bytes."""
+    for (B, Q, N, k) in [(32, 1, 262144, 1024), (1, 1, 262144, 1024), (4, 1, 20001, 1024),
+                         (64, 1, 131072, 1024), (1, 5, 20000, 1024), (255, 1, 20000, 1024)]:
+        p = _p(B=B, k=k)
+        ws = csa.workspace_size(p, csa.WS_TOPK, Q, N)
+        rows = B * Q
+        r256 = lambda x: (x + 255) // 256 * 256
+        lo = r256(rows * 4) + r256(rows * 16 * 4) + r256(rows * N * 8)
+        hi = r256(rows * 4) + r256(rows * 256 * 16 * 4) + r256(rows * N * 8)
+        assert lo <= ws <= hi, (B, Q, N, k, ws)
+    for (B, Q, N, k) in [(2, 3, 16384, 1024), (256, 1, 20000, 1024), (1, 1, 262144, 8192),
+                         (1, 65536, 16384, 1024)]:
+        assert csa.workspace_size(_p(B=B, k=k), csa.WS_TOPK, Q, N) == 0, (B, Q, N, k)
+
+
 def test_debug_stall_aid_validates_its_argument():
     """csa_debug_stall_next touches no GPU state: it only arms a one-shot."""
     from long_context_sparse_25_b300 import csa
